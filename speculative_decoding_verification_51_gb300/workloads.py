@@ -1,0 +1,206 @@
+"""Seeded synthetic inputs for the speculative-sampling verifier.
+
+This module only builds inputs: target logits, a simulated drafter's
+distribution q and its sampled draft tokens, ragged draft counts and
+temperatures.  It holds none of the verifier's arithmetic (no acceptance
+test, no residual, no uniforms) and is shared by the CUDA path's tests, the
+benchmark and the oracle's tests alike.
+
+The five workloads (sizes, value distributions and structure) are the ones
+the verifier is measured on:
+
+  1. B=1,   K=4, V=1024,   f32  logits ~ N(0, 2^2); draft = target + N(0, 1);
+     T = 1.
+  2. B=8,   K=5, V=32000,  bf16 logits ~ N(0, 3^2) with +8 on one random
+     token per row; draft = target + N(0, 1.5^2); odd requests greedy (T=0).
+  3. B=64,  K=4, V=128256, bf16 Zipf(1.1) profile (logit of rank r is
+     -1.1 ln r) placed by one random permutation per request, + N(0, 1) per
+     element; draft = target + N(0, 1); T ~ U[0.5, 1.2].
+  4. B=256, K=3, V=151936, bf16 as 3; num_draft ~ U{0..3}; 25% of requests
+     greedy; draft noise sigma per request from {0.25, 1, 4}; T ~ U[0.5, 1.2].
+  5. B=512, K=8, V=129280, bf16 as 3; draft = target + N(0, 0.5^2);
+     num_draft ~ U{1..8}; T ~ U[0.3, 1.5]; B sweep {32, 128, 512} takes the
+     leading requests.
+
+The drafter: q = softmax(draft_logits / T_b) in float32 (T_b = 1 for greedy
+requests, whose q the verifier never reads); sampling requests draw their
+draft tokens from q, greedy requests take argmax(draft_logits).  Draft ids at
+positions j >= num_draft[b] are set to -1: the verifier must never read them.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+VERIFY_SEED = 0  # Philox seed of the verifier for every workload
+
+
+@dataclass(frozen=True)
+class WorkloadSpec:
+    cid: int
+    B: int
+    K: int
+    V: int
+    dtype: str  # "f32" | "bf16"
+    description: str
+
+
+SPECS = {
+    1: WorkloadSpec(1, 1, 4, 1024, "f32", "B=1 K=4 V=1024 f32 gaussian logits, T=1"),
+    2: WorkloadSpec(2, 8, 5, 32000, "bf16", "B=8 K=5 V=32000 bf16 gaussian+boost, half greedy"),
+    3: WorkloadSpec(3, 64, 4, 128256, "bf16", "B=64 K=4 V=128256 bf16 zipf, T~U[0.5,1.2]"),
+    4: WorkloadSpec(4, 256, 3, 151936, "bf16",
+                    "B=256 K=3 V=151936 bf16 zipf, ragged n~U{0..3}, 25% greedy"),
+    5: WorkloadSpec(5, 512, 8, 129280, "bf16",
+                    "B=512 K=8 V=129280 bf16 zipf, ragged n~U{1..8}, T~U[0.3,1.5]"),
+}
+
+
+@dataclass
+class Workload:
+    spec: WorkloadSpec
+    target_logits: torch.Tensor  # [B, K+1, V] bf16 or f32
+    draft_probs: torch.Tensor    # [B, K, V] f32
+    draft_ids: torch.Tensor      # [B, K] int32 (-1 beyond num_draft)
+    num_draft: torch.Tensor      # [B] int32
+    temperature: torch.Tensor    # [B] f32 (0 = greedy)
+    seed: int = VERIFY_SEED
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def B(self) -> int:
+        return self.target_logits.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.draft_probs.shape[1]
+
+    @property
+    def V(self) -> int:
+        return self.target_logits.shape[2]
+
+    def to(self, device) -> "Workload":
+        return Workload(self.spec, self.target_logits.to(device), self.draft_probs.to(device),
+                        self.draft_ids.to(device), self.num_draft.to(device),
+                        self.temperature.to(device), self.seed, dict(self.meta))
+
+    def subset(self, idx) -> "Workload":
+        """Requests idx (a list or 1-D tensor of request indices)."""
+        i = torch.as_tensor(idx, dtype=torch.long, device=self.target_logits.device)
+        return Workload(self.spec, self.target_logits[i].contiguous(),
+                        self.draft_probs[i].contiguous(), self.draft_ids[i].contiguous(),
+                        self.num_draft[i].contiguous(), self.temperature[i].contiguous(),
+                        self.seed, dict(self.meta))
+
+    def leading(self, B: int) -> "Workload":
+        return self.subset(list(range(B)))
+
+
+def _zipf_logits(B, K1, V, g, device):
+    """-1.1 ln(rank) placed by one permutation per request, + N(0, 1) noise."""
+    rank = torch.arange(1, V + 1, device=device, dtype=torch.float32)
+    base = -1.1 * torch.log(rank)                                   # [V]
+    perm = torch.argsort(torch.rand(B, V, generator=g, device=device), dim=1)
+    placed = torch.empty(B, V, device=device, dtype=torch.float32)
+    placed.scatter_(1, perm, base.expand(B, V).contiguous())        # token perm[r] gets rank r
+    noise = torch.randn(B, K1, V, generator=g, device=device)
+    return placed[:, None, :] + noise
+
+
+def make_workload(cid: int, device="cpu", *, gen_seed: int | None = None, B: int | None = None,
+                  K: int | None = None, V: int | None = None) -> Workload:
+    """Build workload ``cid`` (1..5) on ``device`` from a seeded generator.
+
+    B, K, V override the sizes (for small parity cases of the same recipe).
+    """
+    spec = SPECS[cid]
+    B = spec.B if B is None else B
+    K = spec.K if K is None else K
+    V = spec.V if V is None else V
+    seed = 1000 + cid if gen_seed is None else gen_seed
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    K1 = K + 1
+    f32 = torch.float32
+
+    if cid == 1:
+        target = 2.0 * torch.randn(B, K1, V, generator=g, device=device)
+        draft_noise = torch.ones(B, device=device)
+        num_draft = torch.full((B,), K, dtype=torch.int32, device=device)
+        temp = torch.ones(B, device=device)
+    elif cid == 2:
+        target = 3.0 * torch.randn(B, K1, V, generator=g, device=device)
+        boost = torch.randint(0, V, (B, K1, 1), generator=g, device=device)
+        target.scatter_add_(2, boost, torch.full((B, K1, 1), 8.0, device=device))
+        draft_noise = torch.full((B,), 1.5, device=device)
+        num_draft = torch.full((B,), K, dtype=torch.int32, device=device)
+        temp = torch.ones(B, device=device)
+        temp[1::2] = 0.0  # odd requests greedy
+    elif cid in (3, 4, 5):
+        target = _zipf_logits(B, K1, V, g, device)
+        if cid == 3:
+            draft_noise = torch.ones(B, device=device)
+            num_draft = torch.full((B,), K, dtype=torch.int32, device=device)
+            temp = 0.5 + 0.7 * torch.rand(B, generator=g, device=device)
+        elif cid == 4:
+            sig = torch.tensor([0.25, 1.0, 4.0], device=device)
+            draft_noise = sig[torch.randint(0, 3, (B,), generator=g, device=device)]
+            num_draft = torch.randint(0, K + 1, (B,), generator=g, device=device).to(torch.int32)
+            temp = 0.5 + 0.7 * torch.rand(B, generator=g, device=device)
+            greedy = torch.rand(B, generator=g, device=device) < 0.25
+            temp = torch.where(greedy, torch.zeros_like(temp), temp)
+        else:
+            draft_noise = torch.full((B,), 0.5, device=device)
+            num_draft = torch.randint(1, K + 1, (B,), generator=g, device=device).to(torch.int32)
+            temp = 0.3 + 1.2 * torch.rand(B, generator=g, device=device)
+    else:
+        raise ValueError(f"unknown workload {cid}")
+
+    # the simulated drafter sees the first K rows of the target plus noise
+    dlog = target[:, :K, :] + draft_noise[:, None, None] * torch.randn(
+        B, K, V, generator=g, device=device)
+    t_draft = torch.where(temp > 0, temp, torch.ones_like(temp))
+    draft_probs = torch.softmax(dlog / t_draft[:, None, None], dim=-1).to(f32).contiguous()
+    if K > 0:
+        sampled = torch.multinomial(draft_probs.reshape(B * K, V), 1, generator=g).reshape(B, K)
+        greedy_ids = dlog.argmax(dim=-1)
+        draft_ids = torch.where((temp > 0)[:, None], sampled, greedy_ids).to(torch.int32)
+        pos = torch.arange(K, device=device)[None, :]
+        draft_ids = torch.where(pos < num_draft[:, None].long(), draft_ids,
+                                torch.full_like(draft_ids, -1)).contiguous()
+    else:
+        draft_ids = torch.empty(B, 0, dtype=torch.int32, device=device)
+
+    logits = target.to(torch.bfloat16 if spec.dtype == "bf16" else f32).contiguous()
+    return Workload(spec, logits, draft_probs, draft_ids, num_draft.contiguous(),
+                    temp.to(f32).contiguous(), VERIFY_SEED,
+                    {"gen_seed": seed, "draft_noise": draft_noise.cpu().tolist()
+                     if B <= 16 else None})
+
+
+def to_numpy(w: Workload) -> dict:
+    """Host copies in the layout the oracle takes (bf16 as uint16 bit patterns)."""
+    tl = w.target_logits.detach().cpu()
+    if tl.dtype == torch.bfloat16:
+        tl_np = tl.view(torch.int16).numpy().view("uint16")
+    else:
+        tl_np = tl.numpy()
+    return {
+        "target_logits": tl_np,
+        "draft_probs": w.draft_probs.detach().cpu().numpy(),
+        "draft_ids": w.draft_ids.detach().cpu().numpy(),
+        "num_draft": w.num_draft.detach().cpu().numpy(),
+        "temperature": w.temperature.detach().cpu().numpy(),
+        "seed": w.seed,
+    }
+
+
+def valid_rows(num_draft: torch.Tensor) -> int:
+    """Rows the verifier must read whole: sum_b (num_draft[b] + 1)."""
+    return int((num_draft.long() + 1).sum().item())
+
+
+def positions(num_draft: torch.Tensor) -> int:
+    """Verified draft positions: sum_b num_draft[b]."""
+    return int(num_draft.long().sum().item())
