@@ -1,0 +1,386 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 speculative-sampling verifier.
+
+One step = one spec_verify call over one batch of the largest-vocabulary
+workload (B=256 requests, K=3 drafts, V=151936, bf16 logits, ragged
+num_draft ~ U{0..3}, 25% greedy), inputs resident in HBM.  Prints one JSON
+line (rank 0).
+
+  value     verified draft positions / s (sum_b num_draft[b] per call),
+            device-timed with CUDA events around each call; L2 is flushed
+            (256 MiB write) before every timed call.
+  e2e       same metric through spec_verify_host: pinned host inputs copied
+            in, verified, outputs copied back, all inside the timed region.
+  roofline  k_row_stats (the dominant kernel): algorithmic bytes per launch
+            (every valid logits row once + one 16-byte partial per
+            2048-token chunk) / its CUDA-event duration, against the measured
+            HBM copy bandwidth.
+  cpu_baseline  the float64 oracle on the host cores, on a bounded sample.
+
+--impl reference times the oracle (the only reference this method has) on
+the same workload and prints the same line with "impl": "reference".
+Multi-GPU (torchrun): every rank verifies its own batch of the workload
+(request indices offset by rank * B): weak scaling, no collective on the
+data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "positions/s"
+PEAK_FALLBACK_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+TILE = 2048  # tokens per row-statistics chunk (one 16-byte partial each)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=4, help="workload 1..5 (default 4)")
+    ap.add_argument("--batch", type=int, default=None, help="leading-B subset (sweep)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured", d
+    except Exception:
+        return PEAK_FALLBACK_GBS, "fallback", {}
+
+
+def source_sha(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload_name: str):
+    """ncu DRAM bytes per launch of k_row_stats for this workload, if the
+    committed summary was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "row_stats_traffic.json")
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    src = os.path.join(ROOT, "speculative_decoding_verification_51_gb300", "csrc", "row_stats.cu")
+    if d.get("source_sha") != source_sha(src):
+        return None
+    e = d.get("workloads", {}).get(workload_name)
+    return None if e is None else float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def workload_name(cid, B):
+    return f"config{cid}" + (f"_B{B}" if B else "")
+
+
+def algorithmic_bytes(w, nacc_mode=None):
+    """(row_stats bytes per launch, whole-step algorithmic bytes)."""
+    n = w.num_draft.long().cpu()
+    V, esz = w.V, (2 if w.target_logits.dtype == torch.bfloat16 else 4)
+    rows = int((n + 1).sum())
+    C = (V + TILE - 1) // TILE
+    stats = rows * V * esz + rows * C * 16
+    step = rows * V * esz
+    if nacc_mode is not None:
+        a, greedy = nacc_mode
+        T = w.temperature.cpu()
+        sampling = T > 0
+        resid = int(((a < n) & sampling).sum())
+        step += resid * V * 4                              # q row at the first rejection
+        step += int(n[sampling].sum()) * 4                 # q(x_j) gathers
+    step += w.B * (w.K * 4 + 4 + 4) + w.B * ((w.K + 1) * 4 + 4)  # ids, n, T in; outputs
+    return stats, step
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from speculative_decoding_verification_51_gb300 import workloads as W
+    w = W.make_workload(args.config, device="cpu")
+    if args.batch:
+        w = w.leading(args.batch)
+    inputs = W.to_numpy(w)
+    pos = W.positions(w.num_draft)
+    threads = oracle.omp_threads()
+    oracle.spec_verify(**inputs, n_threads=threads)  # warm (build, page in)
+    for _ in range(max(0, args.warmup - 1)):
+        oracle.spec_verify(**inputs, n_threads=threads)
+    t = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.spec_verify(**inputs, n_threads=threads)
+        t.append(time.perf_counter() - t0)
+    sec = sum(t) / len(t)
+    value = pos / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{workload_name(args.config, args.batch)}: {w.spec.description}",
+                       "B": w.B, "K": w.K, "V": w.V, "positions_per_step": pos},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"the whole batch ({w.B} requests) per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, budget_s):
+    import oracle
+    from speculative_decoding_verification_51_gb300 import workloads as W
+    inputs = W.to_numpy(w)
+    threads = oracle.omp_threads()
+    pos = W.positions(w.num_draft)
+    oracle.spec_verify(**inputs, n_threads=threads)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.spec_verify(**inputs, n_threads=threads)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s or reps >= 50:
+            break
+    sec = (time.perf_counter() - t0) / reps
+    return {"value": pos / sec, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"the whole batch ({w.B} requests, {pos} positions) x {reps} "
+                      f"repetitions, {sec * 1e3:.1f} ms each"}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    from speculative_decoding_verification_51_gb300 import binding
+    from speculative_decoding_verification_51_gb300 import build as _build
+    from speculative_decoding_verification_51_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+    binding.lib()
+
+    w = W.make_workload(args.config, device=dev)
+    if args.batch:
+        w = w.leading(args.batch)
+    B, K, V = w.B, w.K, w.V
+    offset = rank * B  # each rank holds its own requests of the global batch
+    pos = W.positions(w.num_draft)
+    ws = binding.new_workspace(B, K, V, dev)
+    out_ids = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    out_nacc = torch.empty((B,), dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(seed):
+        if offset:
+            binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
+                                w.temperature, seed, out_ids=out_ids, out_num_accepted=out_nacc,
+                                workspace=ws, request_offset=offset)
+        else:
+            binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
+                                w.temperature, seed, out_ids=out_ids, out_num_accepted=out_nacc,
+                                workspace=ws)
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        step(1000 + i)
+    torch.cuda.synchronize()
+
+    # ---- timed region: K calls, device time per call, L2 flushed before each
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_((i + 7) & 0xFF)
+            evs[i][0].record(stream)
+            step(2000 + i)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = clk.summary()
+
+    # ---- per-kernel durations (same workload, marks between the kernels)
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for m in marks:
+        for e in m:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_((i + 3) & 0xFF)
+        binding.spec_verify_profiled(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
+                                     w.temperature, 3000 + i, out_ids, out_nacc, ws, marks[i])
+    torch.cuda.synchronize()
+    kern_ms = [statistics.mean(m[k].elapsed_time(m[k + 1]) for m in marks) for k in range(4)]
+    names = ["k_plan", "k_row_stats", "k_accept", "k_sample"]
+
+    # ---- algorithmic bytes
+    nacc_cpu = out_nacc.cpu().long()
+    stats_bytes, step_bytes = algorithmic_bytes(w, (nacc_cpu, None))
+    peak, peak_kind, _ = measured_peak()
+    ach = stats_bytes / (kern_ms[1] * 1e-3) / 1e9
+    wname = workload_name(args.config, args.batch)
+    roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "traffic": profiled_traffic(wname),
+                "kernel": "k_row_stats", "kernel_ms": round(kern_ms[1], 5),
+                "algorithmic_bytes_per_launch": stats_bytes, "peak_kind": peak_kind}
+
+    # ---- end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        h = {k: getattr(w, k).cpu().pin_memory() for k in
+             ("target_logits", "draft_probs", "draft_ids", "num_draft", "temperature")}
+        h_out = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+        h_nacc = torch.empty((B,), dtype=torch.int32).pin_memory()
+        d_l = torch.empty_like(w.target_logits)
+        d_p = torch.empty_like(w.draft_probs)
+        small = torch.empty(binding.host_small_bytes(B, K), dtype=torch.uint8, device=dev)
+        e2e_steps = max(3, min(args.steps, 10))
+
+        def host_step(seed):
+            binding.spec_verify_host(h["target_logits"], h["draft_probs"], h["draft_ids"],
+                                     h["num_draft"], h["temperature"], seed, h_out, h_nacc, d_l,
+                                     d_p, small, ws)
+
+        for i in range(2):
+            host_step(4000 + i)
+        torch.cuda.synchronize()
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_ev.record(stream)
+        for i in range(e2e_steps):
+            host_step(5000 + i)
+        b_ev.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a_ev.elapsed_time(b_ev) / e2e_steps
+        h2d = sum(t.numel() * t.element_size() for t in h.values())
+        d2h = h_out.numel() * 4 + h_nacc.numel() * 4
+        e2e = {"value": world * pos / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    value = world * pos / (ms * 1e-3)
+    step_gbs = step_bytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{wname}: {w.spec.description}", "B": B, "K": K, "V": V,
+                   "logits_dtype": str(w.target_logits.dtype).replace("torch.", ""),
+                   "positions_per_step": pos, "rows_per_step": W.valid_rows(w.num_draft),
+                   "l2": "flushed before every timed call (256 MiB write)"},
+        "hbm_gbs_step": round(step_gbs, 1), "hbm_frac_step": round(step_gbs / peak, 4),
+        "kernels_ms": {n: round(t, 5) for n, t in zip(names, kern_ms)},
+        "accept_rate": float(nacc_cpu.clamp(min=0).sum()) / max(1, pos),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 4 * args.steps, "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

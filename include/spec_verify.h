@@ -1,0 +1,198 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) batched speculative-sampling
+ * verifier.
+ *
+ * The operation (sources cited by page title and section):
+ *   - "深入推测解码：从概念到实现" (Exploring Speculative Decoding), section
+ *     保证原始分布: accept a drafted token x with probability
+ *     min(1, p(x)/q(x)); on rejection resample from max(0, p(x) - q(x)).
+ *   - "RTP-LLM Speculative Engine 深度解析", section 拒绝采样算法: test the
+ *     drafts in order, stop at the first rejection.
+ *   - "投机采样" (razer666.cn), sections 第三步 to 第五步 of 投机解码算法 and
+ *     the output-length cases: the correction is drawn from
+ *     norm(max(0, p_{n+1} - q_{n+1})); when all gamma drafts are accepted one
+ *     more token is drawn from p_{gamma+1}, so 1..gamma+1 tokens come out;
+ *     section 验收标准 / 精确匹配: the greedy variant accepts a draft iff it is
+ *     the target's most probable token.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor arguments are DEVICE pointers to dense row-major arrays,
+ *     owned by the caller.  The library allocates nothing, keeps no state
+ *     between calls and never synchronises: every call only enqueues work on
+ *     `stream` and returns.
+ *   - Shapes: B requests, K draft positions per request (0 <= K <= 31),
+ *     vocabulary V (8 <= V <= 2^24, V a multiple of 8).
+ *   - Host-checkable errors are returned before anything is enqueued.
+ *   - Data errors are found on the device (see SPEC_BADBIT_*): the offending
+ *     request gets out_ids[b, :] = -1 and out_num_accepted[b] = -1, a bit is
+ *     OR-ed into the device status word, and other requests are unaffected.
+ *     No kernel traps.
+ *   - Calls that share a workspace must not overlap on the GPU (issue them on
+ *     one stream, or order the streams).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st* spec_stream_t;
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1, /* null pointer, negative size, K > 31, ... */
+    SPEC_ERR_UNSUPPORTED = 2, /* V not a multiple of 8, V out of range, misaligned pointer */
+    SPEC_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    SPEC_ERR_WORKSPACE = 4    /* workspace too small or not 256-byte aligned */
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+#define SPEC_MAX_K 31
+
+/* Bits of the device status word (0 when every request was well formed). */
+#define SPEC_BADBIT_NUM_DRAFT 1u   /* num_draft[b] outside [0, K] */
+#define SPEC_BADBIT_TEMPERATURE 2u /* temperature[b] NaN, negative or infinite */
+#define SPEC_BADBIT_DRAFT_ID 4u    /* draft_ids[b, j] outside [0, V) for some j < num_draft[b] */
+#define SPEC_BADBIT_EMPTY_ROW 8u   /* a sampling row j <= num_draft[b] whose logits are all -inf */
+#define SPEC_BADBIT_NO_PROBS 16u   /* a sampling request with drafts but draft_probs == NULL */
+#define SPEC_BADBIT_TIMEOUT 32u    /* an internal bounded wait gave up (never expected) */
+
+/* Human-readable name of a status code (static string). */
+const char* spec_status_str(spec_status s);
+
+/* Bytes of scratch memory spec_verify needs for these sizes (0 on bad sizes).
+ * The workspace must be 256-byte aligned; its contents need no
+ * initialisation and are overwritten by every call. */
+size_t spec_verify_workspace_size(int B, int K, int V);
+
+/*
+ * spec_verify -- verify K drafted tokens for each of B requests.
+ *
+ *   target_logits    [B, K+1, V], dtype logits_dtype (f32 or bf16), 16-byte
+ *                    aligned.  Row (b, j) is the target model's logits for the
+ *                    position that drafted token j would fill; row K (or row
+ *                    num_draft[b]) is the bonus position.  Rows j > num_draft[b]
+ *                    are never read.
+ *   draft_probs      [B, K, V] float32, 16-byte aligned: the draft
+ *                    distribution q_j that drew draft token j, used as given
+ *                    (not renormalised).  Only row e_b (the first rejected
+ *                    position) is read whole; elsewhere only q_j(x_j).  May be
+ *                    NULL when no sampling request has a draft.
+ *   draft_ids        [B, K] int32: x_j; entries j >= num_draft[b] are ignored.
+ *   num_draft        [B] int32: n_b in [0, K] drafts to verify for request b.
+ *   temperature      [B] float32: T_b = 0 selects greedy exact-match
+ *                    verification; T_b > 0 samples from p = softmax(l / T_b).
+ *   seed             Philox4x32-10 key (low word, high word).  Row j of
+ *                    request b draws the block at counter (b, j, 0, 0): lane 0
+ *                    is the acceptance uniform, lane 1 the uniform of a token
+ *                    emitted from that row, each mapped to ((x >> 8) + 1) 2^-24.
+ *                    Change the seed between calls.
+ *   out_ids          [B, K+1] int32 (written): the a_b accepted drafts, then the
+ *                    emitted token (resampled correction, bonus token, or the
+ *                    greedy target token), then -1.
+ *   out_num_accepted [B] int32 (written): a_b in [0, n_b], or -1 for a bad
+ *                    request.
+ *   workspace        scratch of at least spec_verify_workspace_size(B, K, V)
+ *                    bytes, 256-byte aligned; the device status word lives in
+ *                    it (spec_verify_status_ptr).
+ *   stream           stream the kernels are enqueued on.
+ *
+ * Sampling: p_j = softmax(l_j / T_b) is computed in float32 with float64
+ * accumulation; accept x_j iff p_j(x_j) > 0 and (q_j(x_j) == 0 or
+ * u_j <= p_j(x_j) / q_j(x_j)); a_b = the number of leading accepted drafts;
+ * if a_b < n_b the token at a_b is the smallest x with
+ * sum_{y<=x} max(0, p(y) - q(y)) >= u' * sum_y max(0, p(y) - q(y)) on row a_b
+ * (falling back to p if that residual has no mass); if a_b = n_b it is drawn
+ * the same way from p_{n_b}.  Greedy: x_j is accepted iff it is the lowest
+ * index of the maximum of l_j; the emitted token is that argmax of row a_b.
+ */
+spec_status spec_verify(const void* target_logits, spec_dtype logits_dtype,
+                        const float* draft_probs, const int32_t* draft_ids,
+                        const int32_t* num_draft, const float* temperature, uint64_t seed,
+                        int B, int K, int V, int32_t* out_ids, int32_t* out_num_accepted,
+                        void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * spec_verify_ex -- spec_verify plus sharding and diagnostics.
+ *   request_offset  added to b in the Philox counter, so that a shard holding
+ *                   requests [o, o + B) of a larger batch draws the same
+ *                   uniforms as the unsharded call.
+ *   dbg_rows        [B, K+1, 4] float32 or NULL: per row j < n_b of a sampling
+ *                   request {p_j(x_j), u_j, Z_j, accepted (1/0)}, where Z_j =
+ *                   sum_x exp((l_j(x) - max l_j) / T_b); greedy rows give
+ *                   {NaN, NaN, NaN, accepted}; untested rows {NaN, NaN, NaN, -1}.
+ *   dbg_req         [B, 4] float32 or NULL: {mode, emission row, emission mass,
+ *                   u'}; mode -1 bad, 0 greedy, 1 residual, 2 bonus,
+ *                   3 residual without mass (drawn from p).
+ *   dev_status      int32 device word or NULL: receives the status bits of
+ *                   this call (zeroed by the call itself).
+ */
+spec_status spec_verify_ex(const void* target_logits, spec_dtype logits_dtype,
+                           const float* draft_probs, const int32_t* draft_ids,
+                           const int32_t* num_draft, const float* temperature, uint64_t seed,
+                           int B, int K, int V, int32_t* out_ids, int32_t* out_num_accepted,
+                           void* workspace, size_t workspace_bytes, spec_stream_t stream,
+                           uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                           int32_t* dev_status);
+
+/*
+ * spec_verify_profiled -- spec_verify with timing marks: the caller's CUDA
+ * events events[0..4] (cudaEvent_t) are recorded on `stream` before each of
+ * the four kernels of the call (plan, row statistics, acceptance, sampling)
+ * and after the last, so that events[i] -> events[i+1] brackets kernel i.
+ * The marks separate the kernels, which otherwise overlap their launch with
+ * the previous kernel's tail.  Returns SPEC_ERR_INVALID_ARG if any event is
+ * NULL; otherwise as spec_verify.
+ */
+typedef struct CUevent_st* spec_event_t;
+spec_status spec_verify_profiled(const void* target_logits, spec_dtype logits_dtype,
+                                 const float* draft_probs, const int32_t* draft_ids,
+                                 const int32_t* num_draft, const float* temperature,
+                                 uint64_t seed, int B, int K, int V, int32_t* out_ids,
+                                 int32_t* out_num_accepted, void* workspace,
+                                 size_t workspace_bytes, spec_stream_t stream,
+                                 spec_event_t* events);
+
+/* Device address of the status word inside a workspace (no GPU work). */
+int32_t* spec_verify_status_ptr(void* workspace);
+
+/*
+ * spec_verify_host -- spec_verify for callers whose inputs and outputs live in
+ * host memory.  The inputs are copied to the caller's device buffers
+ * (d_logits [B, K+1, V], d_probs [B, K, V], d_small: at least
+ * spec_verify_host_small_bytes(B, K) bytes, 256-byte aligned), the verifier
+ * runs, and out_ids / out_num_accepted are copied back, all enqueued on
+ * `stream` in that order (one cudaMemcpyAsync per tensor).  Host buffers
+ * should be pinned for the copies to be asynchronous; the call does not
+ * synchronise, so the host outputs are valid after the stream is synchronised.
+ * h_probs / d_probs may be NULL when every request is greedy.
+ */
+size_t spec_verify_host_small_bytes(int B, int K);
+spec_status spec_verify_host(const void* h_logits, spec_dtype logits_dtype, const float* h_probs,
+                             const int32_t* h_draft_ids, const int32_t* h_num_draft,
+                             const float* h_temperature, uint64_t seed, int B, int K, int V,
+                             int32_t* h_out_ids, int32_t* h_out_num_accepted, void* d_logits,
+                             float* d_probs, void* d_small, void* workspace,
+                             size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * spec_philox_fill -- the library's Philox4x32-10 for cross-checking:
+ * out[4i..4i+3] = Philox4x32-10(counter = ctrs[4i..4i+3], key = (seed lo,
+ * seed hi)) for i < n.  ctrs and out are device arrays of 4n uint32.
+ * Source: J. Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3",
+ * SC'11 (Philox4x32 with 10 rounds).
+ */
+spec_status spec_philox_fill(uint64_t seed, const uint32_t* ctrs, int64_t n, uint32_t* out,
+                             spec_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

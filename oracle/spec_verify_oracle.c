@@ -381,8 +381,8 @@ int oracle_spec_verify(const void* target_logits, int logits_dtype, const float*
                 }
             }
             int rc = -1;
-            if (draft_probs != NULL || temperature[b] == 0.0f) {
-                /* greedy requests read no draft probabilities */
+            if (draft_probs != NULL || temperature[b] == 0.0f || num_draft[b] == 0) {
+                /* greedy requests, and requests without drafts, read no q */
                 rc = verify_request(target_logits, logits_dtype, draft_probs,
                                     draft_ids + (size_t)b * (size_t)K, num_draft[b],
                                     temperature[b], b, K, V, ua, ue,

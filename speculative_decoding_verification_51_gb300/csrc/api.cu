@@ -1,0 +1,305 @@
+// api.cu -- the C ABI declared in include/spec_verify.h: argument checks,
+// workspace carving and the launch sequence of one verification call.
+#include <cfloat>
+#include <mutex>
+
+#include "common.cuh"
+
+using namespace sv;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int stats_blocks_bf16 = 0;  // resident k_row_stats CTAs per SM
+    int stats_blocks_f32 = 0;
+    int sample_blocks = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+constexpr size_t stats_smem(int dtype) {
+    return size_t(STATS_WARPS) * STATS_STAGES * TILE * (dtype == SPEC_BF16 ? 2 : 4);
+}
+
+// Per-device launch facts, computed once per device (thread-safe).
+spec_status device_info(DeviceInfo& out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+        if (cudaFuncSetAttribute(k_row_stats_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(stats_smem(SPEC_BF16))) != cudaSuccess ||
+            cudaFuncSetAttribute(k_row_stats_f32, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(stats_smem(SPEC_F32))) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.stats_blocks_bf16,
+                                                          k_row_stats_bf16, STATS_WARPS * 32,
+                                                          stats_smem(SPEC_BF16)) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.stats_blocks_f32,
+                                                          k_row_stats_f32, STATS_WARPS * 32,
+                                                          stats_smem(SPEC_F32)) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sample_blocks, k_sample_bf16,
+                                                          SAMPLE_THREADS, 0) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+        d.stats_blocks_bf16 = d.stats_blocks_bf16 < 1 ? 1 : d.stats_blocks_bf16;
+        d.stats_blocks_f32 = d.stats_blocks_f32 < 1 ? 1 : d.stats_blocks_f32;
+        d.sample_blocks = d.sample_blocks < 1 ? 1 : (d.sample_blocks > 4 ? 4 : d.sample_blocks);
+        d.ready = true;
+    }
+    out = d;
+    return SPEC_OK;
+}
+
+cudaError_t launch(void (*kern)(Params), unsigned grid, unsigned block, size_t smem,
+                   cudaStream_t st, bool pdl, const Params& P) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+bool sizes_ok(int B, int K, int V) {
+    return B >= 0 && B <= (1 << 24) && K >= 0 && K <= SPEC_MAX_K && V >= 8 && V <= (1 << 24);
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+}  // namespace
+
+static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtype,
+                           const float* draft_probs, const int32_t* draft_ids,
+                           const int32_t* num_draft, const float* temperature, uint64_t seed,
+                           int B, int K, int V, int32_t* out_ids, int32_t* out_num_accepted,
+                           void* workspace, size_t workspace_bytes, spec_stream_t stream,
+                           uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                           int32_t* dev_status, cudaEvent_t* events) {
+    if (!sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
+    if (logits_dtype != SPEC_F32 && logits_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+    if (V % 8 != 0) return SPEC_ERR_UNSUPPORTED;
+    if (B == 0) return SPEC_OK;
+    if (!target_logits || !num_draft || !temperature || !out_ids || !out_num_accepted ||
+        !workspace || (K > 0 && !draft_ids))
+        return SPEC_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(target_logits) & 15) ||
+        (reinterpret_cast<uintptr_t>(draft_probs) & 15))
+        return SPEC_ERR_UNSUPPORTED;
+    const Layout L = make_layout(B, K, V);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) || workspace_bytes < L.total)
+        return SPEC_ERR_WORKSPACE;
+
+    DeviceInfo dev;
+    if (device_info(dev) != SPEC_OK) return SPEC_ERR_CUDA;
+
+    Params P;
+    P.logits = target_logits;
+    P.probs = draft_probs;
+    P.ids = draft_ids;
+    P.num_draft = num_draft;
+    P.temp = temperature;
+    P.out_ids = out_ids;
+    P.out_nacc = out_num_accepted;
+    P.dbg_rows = dbg_rows;
+    P.dbg_req = dbg_req;
+    P.hdr = at<int>(workspace, L.hdr);
+    P.status = dev_status ? dev_status : P.hdr + HDR_STATUS;
+    P.rowlist = at<int>(workspace, L.rowlist);
+    P.req_flags = at<int>(workspace, L.req_flags);
+    P.part = at<Partial>(workspace, L.part);
+    P.reqs = at<ReqRec>(workspace, L.reqs);
+    P.res_list = at<int>(workspace, L.res_list);
+    P.bonus_list = at<int>(workspace, L.bonus_list);
+    P.res_cnt = at<int>(workspace, L.res_cnt);
+    P.rsum = at<double>(workspace, L.rsum);
+    P.seed = seed;
+    P.req_off = request_offset;
+    P.dtype = logits_dtype;
+    P.B = B;
+    P.K = K;
+    P.K1 = K + 1;
+    P.V = V;
+    P.C = (V + TILE - 1) / TILE;
+    P.C2 = (V + CH2 - 1) / CH2;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const bool bf16 = logits_dtype == SPEC_BF16;
+    const long long max_tiles = (long long)B * P.K1 * P.C;
+    long long g1 = (long long)dev.sms * (bf16 ? dev.stats_blocks_bf16 : dev.stats_blocks_f32);
+    const long long need1 = (max_tiles + STATS_WARPS - 1) / STATS_WARPS;
+    if (g1 > need1) g1 = need1;
+    const unsigned g2 = unsigned((B + ACCEPT_WARPS - 1) / ACCEPT_WARPS);
+    long long g3 = (long long)dev.sms * dev.sample_blocks;
+    const long long need3 = (long long)B * P.C2 + B;
+    if (g3 > need3) g3 = need3;
+
+    // events (profiling only) are recorded before each kernel and after the last
+    auto mark = [&](int i) { return events ? cudaEventRecord(events[i], st) : cudaSuccess; };
+    cudaError_t e = mark(0);
+    if (e == cudaSuccess) e = launch(k_plan, 1, PLAN_THREADS, 0, st, false, P);
+    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess)
+        e = launch(bf16 ? k_row_stats_bf16 : k_row_stats_f32, unsigned(g1),
+                   STATS_WARPS * 32, stats_smem(logits_dtype), st, true, P);
+    if (e == cudaSuccess) e = mark(2);
+    if (e == cudaSuccess) e = launch(k_accept, g2, ACCEPT_WARPS * 32, 0, st, true, P);
+    if (e == cudaSuccess) e = mark(3);
+    if (e == cudaSuccess)
+        e = launch(bf16 ? k_sample_bf16 : k_sample_f32, unsigned(g3), SAMPLE_THREADS,
+                   0, st, true, P);
+    if (e == cudaSuccess) e = mark(4);
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+extern "C" {
+
+const char* spec_status_str(spec_status s) {
+    switch (s) {
+        case SPEC_OK: return "SPEC_OK";
+        case SPEC_ERR_INVALID_ARG: return "SPEC_ERR_INVALID_ARG";
+        case SPEC_ERR_UNSUPPORTED: return "SPEC_ERR_UNSUPPORTED";
+        case SPEC_ERR_CUDA: return "SPEC_ERR_CUDA";
+        case SPEC_ERR_WORKSPACE: return "SPEC_ERR_WORKSPACE";
+    }
+    return "SPEC_ERR_UNKNOWN";
+}
+
+size_t spec_verify_workspace_size(int B, int K, int V) {
+    if (!sizes_ok(B, K, V) || V % 8 != 0) return 0;
+    return make_layout(B, K, V).total;
+}
+
+int32_t* spec_verify_status_ptr(void* workspace) {
+    return workspace ? at<int32_t>(workspace, 0) + HDR_STATUS : nullptr;
+}
+
+spec_status spec_verify_ex(const void* target_logits, spec_dtype logits_dtype,
+                           const float* draft_probs, const int32_t* draft_ids,
+                           const int32_t* num_draft, const float* temperature, uint64_t seed,
+                           int B, int K, int V, int32_t* out_ids, int32_t* out_num_accepted,
+                           void* workspace, size_t workspace_bytes, spec_stream_t stream,
+                           uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                           int32_t* dev_status) {
+    return verify_impl(target_logits, logits_dtype, draft_probs, draft_ids, num_draft,
+                       temperature, seed, B, K, V, out_ids, out_num_accepted, workspace,
+                       workspace_bytes, stream, request_offset, dbg_rows, dbg_req, dev_status,
+                       nullptr);
+}
+
+spec_status spec_verify_profiled(const void* target_logits, spec_dtype logits_dtype,
+                                 const float* draft_probs, const int32_t* draft_ids,
+                                 const int32_t* num_draft, const float* temperature,
+                                 uint64_t seed, int B, int K, int V, int32_t* out_ids,
+                                 int32_t* out_num_accepted, void* workspace,
+                                 size_t workspace_bytes, spec_stream_t stream,
+                                 spec_event_t* events) {
+    if (!events) return SPEC_ERR_INVALID_ARG;
+    for (int i = 0; i < 5; ++i)
+        if (!events[i]) return SPEC_ERR_INVALID_ARG;
+    return verify_impl(target_logits, logits_dtype, draft_probs, draft_ids, num_draft,
+                       temperature, seed, B, K, V, out_ids, out_num_accepted, workspace,
+                       workspace_bytes, stream, 0u, nullptr, nullptr, nullptr,
+                       reinterpret_cast<cudaEvent_t*>(events));
+}
+
+spec_status spec_verify(const void* target_logits, spec_dtype logits_dtype,
+                        const float* draft_probs, const int32_t* draft_ids,
+                        const int32_t* num_draft, const float* temperature, uint64_t seed, int B,
+                        int K, int V, int32_t* out_ids, int32_t* out_num_accepted,
+                        void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+    return spec_verify_ex(target_logits, logits_dtype, draft_probs, draft_ids, num_draft,
+                          temperature, seed, B, K, V, out_ids, out_num_accepted, workspace,
+                          workspace_bytes, stream, 0u, nullptr, nullptr, nullptr);
+}
+
+// Small device buffer of spec_verify_host: ids, num_draft, temperature,
+// out_ids, out_num_accepted, each 256-byte aligned.
+size_t spec_verify_host_small_bytes(int B, int K) {
+    if (B < 0 || K < 0 || K > SPEC_MAX_K) return 0;
+    const size_t b = size_t(B), k1 = size_t(K) + 1;
+    return align256(b * K * 4) + align256(b * 4) + align256(b * 4) + align256(b * k1 * 4) +
+           align256(b * 4);
+}
+
+spec_status spec_verify_host(const void* h_logits, spec_dtype logits_dtype, const float* h_probs,
+                             const int32_t* h_draft_ids, const int32_t* h_num_draft,
+                             const float* h_temperature, uint64_t seed, int B, int K, int V,
+                             int32_t* h_out_ids, int32_t* h_out_num_accepted, void* d_logits,
+                             float* d_probs, void* d_small, void* workspace,
+                             size_t workspace_bytes, spec_stream_t stream) {
+    if (!sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
+    if (logits_dtype != SPEC_F32 && logits_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+    if (V % 8 != 0) return SPEC_ERR_UNSUPPORTED;
+    if (B == 0) return SPEC_OK;
+    if (!h_logits || !h_num_draft || !h_temperature || !h_out_ids || !h_out_num_accepted ||
+        !d_logits || !d_small || (K > 0 && !h_draft_ids) || (h_probs && !d_probs))
+        return SPEC_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(d_small) & 255) return SPEC_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t b = size_t(B), k1 = size_t(K) + 1, esz = logits_dtype == SPEC_BF16 ? 2 : 4;
+    char* s = static_cast<char*>(d_small);
+    int32_t* d_ids = reinterpret_cast<int32_t*>(s);
+    s += align256(b * K * 4);
+    int32_t* d_num = reinterpret_cast<int32_t*>(s);
+    s += align256(b * 4);
+    float* d_temp = reinterpret_cast<float*>(s);
+    s += align256(b * 4);
+    int32_t* d_out = reinterpret_cast<int32_t*>(s);
+    s += align256(b * k1 * 4);
+    int32_t* d_nacc = reinterpret_cast<int32_t*>(s);
+
+    cudaError_t e = cudaMemcpyAsync(d_logits, h_logits, b * k1 * V * esz, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && h_probs)
+        e = cudaMemcpyAsync(d_probs, h_probs, b * K * V * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && K > 0)
+        e = cudaMemcpyAsync(d_ids, h_draft_ids, b * K * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(d_num, h_num_draft, b * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(d_temp, h_temperature, b * 4, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return SPEC_ERR_CUDA;
+    const spec_status r = spec_verify(d_logits, logits_dtype, h_probs ? d_probs : nullptr,
+                                      K > 0 ? d_ids : nullptr, d_num, d_temp, seed, B, K, V,
+                                      d_out, d_nacc, workspace, workspace_bytes, stream);
+    if (r != SPEC_OK) return r;
+    e = cudaMemcpyAsync(h_out_ids, d_out, b * k1 * 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(h_out_num_accepted, d_nacc, b * 4, cudaMemcpyDeviceToHost, st);
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status spec_philox_fill(uint64_t seed, const uint32_t* ctrs, int64_t n, uint32_t* out,
+                             spec_stream_t stream) {
+    if (n < 0 || (n > 0 && (!ctrs || !out))) return SPEC_ERR_INVALID_ARG;
+    if (n == 0) return SPEC_OK;
+    const long long blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    k_philox_fill<<<unsigned(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(seed, ctrs,
+                                                                                      n, out);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace sv {
+__global__ void k_philox_fill(uint64_t seed, const uint32_t* ctrs, int64_t n, uint32_t* out) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 c = reinterpret_cast<const uint4*>(ctrs)[i];
+        reinterpret_cast<uint4*>(out)[i] = philox4x32_10(c, uint32_t(seed), uint32_t(seed >> 32));
+    }
+}
+}  // namespace sv

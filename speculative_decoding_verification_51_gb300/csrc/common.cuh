@@ -1,0 +1,265 @@
+// common.cuh -- shared definitions of the spec_verify kernels (sm_103a).
+//
+// Pipeline of one spec_verify call (all on the caller's stream):
+//   k_plan       1 CTA: validate num_draft / temperature, compact the rows
+//                every request needs (j = 0..n_b) into a row list.
+//   k_row_stats  persistent, one independent bulk-copy pipeline per warp: for
+//                every (valid row, 2048-token chunk) the chunk max, the sum of
+//                exp2((l - max) * log2(e) / T) and (greedy rows) the argmax.
+//   k_accept     one warp per request: merge the chunk partials into per-row
+//                (max, Z, argmax), gather l(x_j) and q(x_j), draw Philox
+//                uniforms, acceptance bits, first-reject scan (ballot), write
+//                the accepted prefix; queue sampling requests.
+//   k_sample     persistent: residual chunk sums over the first rejected row,
+//                then (last CTA per request) the two-level inverse CDF; bonus
+//                tokens by the same inverse CDF over the row-stat partials.
+// Kernels after k_plan are launched with programmatic dependent launch; each
+// CTA executes griddepcontrol.wait before it touches its predecessor's output.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "spec_verify.h"
+
+namespace sv {
+
+// ---------------------------------------------------------------- sizes
+
+constexpr int TILE = 2048;           // tokens per row-stat chunk (one warp tile)
+constexpr int STATS_WARPS = 8;       // warps per k_row_stats CTA
+constexpr int STATS_STAGES = 3;      // bulk-copy stages per warp
+constexpr int CH2 = 8192;            // tokens per residual chunk (one CTA unit)
+constexpr int SAMPLE_THREADS = 256;  // k_sample CTA
+constexpr int ACCEPT_WARPS = 8;      // requests per k_accept CTA
+constexpr int PLAN_THREADS = 1024;
+
+enum { HDR_ROWS = 0, HDR_NRES = 1, HDR_NBONUS = 2, HDR_STATUS = 3, HDR_INTS = 64 };
+enum { MODE_BAD = -1, MODE_GREEDY = 0, MODE_RESIDUAL = 1, MODE_BONUS = 2, MODE_FALLBACK = 3 };
+
+// Per (row, chunk) statistics written by k_row_stats.
+struct __align__(16) Partial {
+    float m;     // max of the raw logits in the chunk (-inf if none finite)
+    int amax;    // greedy rows: lowest token index attaining m; else -1
+    double z;    // sampling rows: sum exp2((l - m) * kappa) over the chunk
+};
+
+// Per request decision written by k_accept for sampling requests.
+struct __align__(16) ReqRec {
+    int mode;     // MODE_*
+    int erow;     // row the emitted token is drawn from
+    float m;      // max of the raw logits of row erow
+    float kappa;  // log2(e) / T (clamped to FLT_MAX)
+    double Z;     // sum_x exp2((l(x) - m) * kappa) over row erow
+    float u2;     // emission uniform of row erow (Philox lane 1)
+    int b;        // request index
+};
+
+struct Params {
+    const void* logits;
+    const float* probs;
+    const int32_t* ids;
+    const int32_t* num_draft;
+    const float* temp;
+    int32_t* out_ids;
+    int32_t* out_nacc;
+    float* dbg_rows;
+    float* dbg_req;
+    int32_t* status;  // device status word (bits SPEC_BADBIT_*)
+    // workspace sections
+    int* hdr;
+    int* rowlist;     // [B*(K+1)] slot = b*(K+1)+j of each compacted row
+    int* req_flags;   // [B] bad bits found by k_plan
+    Partial* part;    // [B*(K+1)*C]
+    ReqRec* reqs;     // [B]
+    int* res_list;    // [B]
+    int* bonus_list;  // [B]
+    int* res_cnt;     // [B] finished residual chunks per queued request
+    double* rsum;     // [B*C2] residual chunk sums
+    uint64_t seed;
+    uint32_t req_off;
+    int dtype;  // SPEC_F32 / SPEC_BF16
+    int B, K, K1, V;
+    int C;   // ceil(V / TILE)
+    int C2;  // ceil(V / CH2)
+};
+
+// Workspace layout (byte offsets, each section 256-byte aligned).
+struct Layout {
+    size_t hdr, rowlist, req_flags, part, reqs, res_list, bonus_list, res_cnt, rsum, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline Layout make_layout(int B, int K, int V) {
+    Layout L;
+    const size_t K1 = size_t(K) + 1, C = (size_t(V) + TILE - 1) / TILE,
+                 C2 = (size_t(V) + CH2 - 1) / CH2;
+    size_t o = 0;
+    L.hdr = o;        o = align256(o + HDR_INTS * sizeof(int));
+    L.rowlist = o;    o = align256(o + size_t(B) * K1 * sizeof(int));
+    L.req_flags = o;  o = align256(o + size_t(B) * sizeof(int));
+    L.part = o;       o = align256(o + size_t(B) * K1 * C * sizeof(Partial));
+    L.reqs = o;       o = align256(o + size_t(B) * sizeof(ReqRec));
+    L.res_list = o;   o = align256(o + size_t(B) * sizeof(int));
+    L.bonus_list = o; o = align256(o + size_t(B) * sizeof(int));
+    L.res_cnt = o;    o = align256(o + size_t(B) * sizeof(int));
+    L.rsum = o;       o = align256(o + size_t(B) * C2 * sizeof(double));
+    L.total = o;
+    return L;
+}
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase: false if it did not complete within
+// `limit_ns` (the caller then reports SPEC_BADBIT_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
+
+// 2^x on the SFU (relative error a few ulp; 0 for x = -inf).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// log2(e) / T, clamped so that (l - m) * kappa stays 0 at l == m.
+__device__ __forceinline__ float kappa_of(float T) {
+    const float k = 1.4426950408889634f / T;
+    return k < 3.4028234663852886e38f ? k : 3.4028234663852886e38f;
+}
+
+// One logit as float (bf16 is the top half of an f32).
+__device__ __forceinline__ float load_logit(const void* logits, int dtype, size_t idx) {
+    if (dtype == SPEC_BF16) {
+        const uint16_t h = __ldg(reinterpret_cast<const unsigned short*>(logits) + idx);
+        return __uint_as_float(uint32_t(h) << 16);
+    }
+    return __ldg(reinterpret_cast<const float*>(logits) + idx);
+}
+
+// ---------------------------------------------------------------- Philox4x32-10
+// J. Salmon, M. Moraes, R. Dror, D. Shaw, "Parallel Random Numbers: As Easy as
+// 1, 2, 3" (SC'11): ten rounds of two 32x32->64 multiplies with the key bumped
+// by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+// 32 random bits -> (0, 1]: ((x >> 8) + 1) * 2^-24 (exact in float).
+__device__ __forceinline__ float uniform01(uint32_t x) {
+    return float((x >> 8) + 1u) * 5.9604644775390625e-8f;
+}
+// Uniforms of row j of request b (global index b + req_off).
+__device__ __forceinline__ uint4 row_block(const Params& P, int b, int j) {
+    return philox4x32_10(make_uint4(uint32_t(b) + P.req_off, uint32_t(j), 0u, 0u),
+                         uint32_t(P.seed), uint32_t(P.seed >> 32));
+}
+
+// ---------------------------------------------------------------- reductions
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ int warp_min_int(int v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ int warp_max_int(int v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Kernel entry points (defined in the .cu files).
+__global__ void k_plan(Params P);
+__global__ void k_row_stats_f32(Params P);
+__global__ void k_row_stats_bf16(Params P);
+__global__ void k_accept(Params P);
+__global__ void k_sample_f32(Params P);
+__global__ void k_sample_bf16(Params P);
+__global__ void k_philox_fill(uint64_t seed, const uint32_t* ctrs, int64_t n, uint32_t* out);
+
+}  // namespace sv

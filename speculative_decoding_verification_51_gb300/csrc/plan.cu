@@ -1,0 +1,71 @@
+// plan.cu -- k_plan: validate the per-request scalars and compact the rows the
+// verifier must read.
+//
+// Request b needs rows j = 0..n_b of its target logits: rows 0..n_b-1 for the
+// acceptance tests of its drafts and row n_b for the bonus token ("投机采样",
+// 第二步: one target pass yields p_1..p_{gamma+1}).  Requests with a bad
+// num_draft or temperature contribute no rows and are flagged.
+#include <cfloat>
+
+#include "common.cuh"
+
+namespace sv {
+
+__global__ void __launch_bounds__(PLAN_THREADS) k_plan(Params P) {
+    __shared__ int warp_excl[PLAN_THREADS / 32];
+    __shared__ int carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    griddep_launch_dependents();
+    if (tid == 0) {
+        P.hdr[HDR_NRES] = 0;
+        P.hdr[HDR_NBONUS] = 0;
+        *P.status = 0;
+        carry = 0;
+    }
+    __syncthreads();
+    int flags_any = 0;
+    for (int base = 0; base < P.B; base += PLAN_THREADS) {
+        const int b = base + tid;
+        int rows = 0;
+        if (b < P.B) {
+            const int n = P.num_draft[b];
+            const float T = P.temp[b];
+            int flags = 0;
+            if (n < 0 || n > P.K) flags |= SPEC_BADBIT_NUM_DRAFT;
+            if (!(T >= 0.f) || T > FLT_MAX) flags |= SPEC_BADBIT_TEMPERATURE;
+            if (!flags && T > 0.f && n > 0 && P.probs == nullptr) flags |= SPEC_BADBIT_NO_PROBS;
+            rows = flags ? 0 : n + 1;
+            P.req_flags[b] = flags;
+            flags_any |= flags;
+        }
+        // block-wide exclusive scan of the row counts
+        int incl = rows;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) warp_excl[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int tot = warp_excl[lane];
+            int s = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += v;
+            }
+            warp_excl[lane] = s - tot;
+        }
+        __syncthreads();
+        const int start = carry + warp_excl[warp] + incl - rows;
+        for (int j = 0; j < rows; ++j) P.rowlist[start + j] = b * P.K1 + j;
+        __syncthreads();
+        if (tid == PLAN_THREADS - 1) carry = start + rows;
+        __syncthreads();
+    }
+    if (flags_any) atomicOr(P.status, flags_any);
+    if (tid == 0) P.hdr[HDR_ROWS] = carry;
+}
+
+}  // namespace sv

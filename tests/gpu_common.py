@@ -1,0 +1,66 @@
+"""Helpers shared by the GPU tests: run the CUDA path and the oracle on the
+same seeded inputs."""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+import torch
+
+import oracle
+import parity
+from speculative_decoding_verification_51_gb300 import binding
+from speculative_decoding_verification_51_gb300 import build as _build
+from speculative_decoding_verification_51_gb300 import workloads as W
+
+_BUILT = False
+
+
+def ensure_built():
+    global _BUILT
+    if not _BUILT:
+        _build.build()
+        binding.lib()
+        _BUILT = True
+
+
+def run_gpu(w: W.Workload, debug=True, **kw):
+    ensure_built()
+    res = binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
+                              w.temperature, w.seed, debug=debug, **kw)
+    torch.cuda.synchronize()
+    return [None if t is None else t.cpu().numpy() for t in res]
+
+
+def check_parity(w: W.Workload, tag: str, **kw) -> parity.Report:
+    inputs = W.to_numpy(w)
+    ids, nacc, rows, _ = run_gpu(w, **kw)
+    ref = oracle.spec_verify(**inputs)
+    rep = parity.compare(inputs, ids, nacc, rows, ref)
+    print(f"[{tag}] {rep.summary()}")
+    d = os.environ.get("PARITY_REPORT_DIR")
+    if d:
+        os.makedirs(d, exist_ok=True)
+        with open(os.path.join(d, f"parity_{tag}.json"), "w") as f:
+            json.dump({"tag": tag, "summary": rep.summary(), "requests": rep.requests,
+                       "rows": rep.rows, "excused_accept": rep.excused_accept,
+                       "excused_cdf": rep.excused_cdf, "max_p_rel": rep.max_p_rel,
+                       "failures": [str(x) for x in rep.failures[:20]]}, f, indent=1)
+    return rep
+
+
+def custom_workload(logits: np.ndarray, probs: np.ndarray | None, ids, num, temp, *,
+                    bf16: bool, seed: int = 0, device="cuda") -> W.Workload:
+    """A workload from explicit host arrays (logits as float values)."""
+    t = torch.from_numpy(np.ascontiguousarray(logits, dtype=np.float32))
+    t = t.to(torch.bfloat16) if bf16 else t
+    B, K1, V = t.shape
+    K = K1 - 1
+    q = (torch.from_numpy(np.ascontiguousarray(probs, dtype=np.float32)) if probs is not None
+         else torch.zeros((B, K, V), dtype=torch.float32))
+    spec = W.WorkloadSpec(0, B, K, V, "bf16" if bf16 else "f32", "custom")
+    return W.Workload(spec, t.to(device).contiguous(), q.to(device).contiguous(),
+                      torch.as_tensor(np.asarray(ids, np.int32).reshape(B, K)).to(device),
+                      torch.as_tensor(np.asarray(num, np.int32).reshape(B)).to(device),
+                      torch.as_tensor(np.asarray(temp, np.float32).reshape(B)).to(device), seed)

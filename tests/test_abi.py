@@ -1,0 +1,82 @@
+"""The C-ABI library loads, exports every declared entry point, and rejects
+bad arguments on the host before touching a GPU (CPU only: no call here
+reaches CUDA)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and
+                                not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="needs nvcc to build the library")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_51_gb300 import binding, build
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size",
+              "spec_verify_host", "spec_philox_fill", "spec_status_str"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in spec_verify.h but not exported"
+
+
+def test_workspace_size(lib):
+    from speculative_decoding_verification_51_gb300 import binding
+    assert binding.workspace_size(4, 3, 1024) > 0
+    assert binding.workspace_size(256, 3, 151936) >= 256 * 4 * 75 * 16  # one partial per chunk
+    assert binding.workspace_size(-1, 3, 1024) == 0
+    assert binding.workspace_size(4, 32, 1024) == 0   # K above 31
+    assert binding.workspace_size(4, 3, 1020) == 0    # V not a multiple of 8
+    assert binding.workspace_size(4, 3, 4) == 0       # V below 8
+
+
+def _call(lib, B=2, K=3, V=64, logits=0x10000, dtype=1, probs=0x20000, ids=0x30000,
+          num=0x40000, temp=0x50000, out=0x60000, nacc=0x70000, ws=0x80000, ws_bytes=1 << 30):
+    vp = ctypes.c_void_p
+    return lib.spec_verify(vp(logits), dtype, vp(probs), vp(ids), vp(num), vp(temp),
+                           ctypes.c_uint64(0), B, K, V, vp(out), vp(nacc), vp(ws), ws_bytes,
+                           vp(0))
+
+
+def test_host_side_errors(lib):
+    from speculative_decoding_verification_51_gb300 import binding as bd
+    assert _call(lib, B=-1) == bd.SPEC_ERR_INVALID_ARG
+    assert _call(lib, K=32) == bd.SPEC_ERR_INVALID_ARG
+    assert _call(lib, V=4) == bd.SPEC_ERR_INVALID_ARG
+    assert _call(lib, dtype=7) == bd.SPEC_ERR_INVALID_ARG
+    assert _call(lib, V=1020) == bd.SPEC_ERR_UNSUPPORTED
+    assert _call(lib, B=0) == bd.SPEC_OK            # nothing to do, nothing enqueued
+    assert _call(lib, logits=0) == bd.SPEC_ERR_INVALID_ARG
+    assert _call(lib, num=0) == bd.SPEC_ERR_INVALID_ARG
+    assert _call(lib, ids=0) == bd.SPEC_ERR_INVALID_ARG
+    assert _call(lib, ws=0) == bd.SPEC_ERR_INVALID_ARG
+    assert _call(lib, logits=0x10008) == bd.SPEC_ERR_UNSUPPORTED   # not 16-byte aligned
+    assert _call(lib, probs=0x20004) == bd.SPEC_ERR_UNSUPPORTED
+    assert _call(lib, ws=0x80010) == bd.SPEC_ERR_WORKSPACE         # not 256-byte aligned
+    assert _call(lib, ws_bytes=16) == bd.SPEC_ERR_WORKSPACE
+    assert lib.spec_philox_fill(0, None, -1, None, None) == bd.SPEC_ERR_INVALID_ARG
+    assert lib.spec_philox_fill(0, None, 0, None, None) == bd.SPEC_OK
+    assert lib.spec_status_str(4) == b"SPEC_ERR_WORKSPACE"
+    assert lib.spec_verify_status_ptr(ctypes.c_void_p(0x1000)) == 0x100C
+    assert bd.host_small_bytes(3, 2) == 5 * 256
