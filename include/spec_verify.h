@@ -159,6 +159,37 @@ spec_status spec_verify_profiled(const void* target_logits, spec_dtype logits_dt
                                  size_t workspace_bytes, spec_stream_t stream,
                                  spec_event_t* events);
 
+/*
+ * spec_verify_noalloc -- spec_verify without a caller-provided workspace, for
+ * callers that must not allocate device memory at all: for example code
+ * running inside an engine that has already handed every byte of the GPU to
+ * its own pools (weights, KV cache) and forbids further cudaMalloc, or a
+ * plugin whose host passes it only its input and output buffers.  For them a
+ * cudaMalloc either fails or stalls the device in the middle of a decoding
+ * step.  (The source pages describe no such entry point; it is an addition of
+ * this library.)
+ *
+ * Arguments and results are those of spec_verify.  The scratch memory is one
+ * array of SPEC_NOALLOC_SCRATCH_BYTES bytes of static device memory inside the
+ * library, present on every GPU that loads the library until the process
+ * exits; this call allocates nothing.  Sizes whose workspace
+ * (spec_verify_workspace_size) exceeds SPEC_NOALLOC_SCRATCH_BYTES are rejected
+ * with SPEC_ERR_WORKSPACE before anything is enqueued.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls on a device share the one array: calls that overlap on
+ * the GPU (different streams, not ordered) race on it and give undefined
+ * results.  The array keeps the previous call's contents, which the kernels
+ * never rely on (every call rewrites what it reads).
+ */
+#define SPEC_NOALLOC_SCRATCH_BYTES (8u << 20)
+spec_status spec_verify_noalloc(const void* target_logits, spec_dtype logits_dtype,
+                                const float* draft_probs, const int32_t* draft_ids,
+                                const int32_t* num_draft, const float* temperature, uint64_t seed,
+                                int B, int K, int V, int32_t* out_ids, int32_t* out_num_accepted,
+                                spec_stream_t stream);
+
 /* Device address of the status word inside a workspace (no GPU work). */
 int32_t* spec_verify_status_ptr(void* workspace);
 

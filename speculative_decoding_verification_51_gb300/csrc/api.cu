@@ -282,6 +282,46 @@ spec_status spec_verify_host(const void* h_logits, spec_dtype logits_dtype, cons
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+// spec_verify_noalloc: spec_verify for callers that cannot allocate device
+// memory.  Its scratch is the file-scope array below, created with the module
+// on every GPU that loads this library and kept until the process exits.
+// Host code only ever sees a host-side stand-in for the array's name, so the
+// device address is looked up once per device (cudaGetSymbolAddress, with
+// that device current) on the first call made on that device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
+
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[kMaxDevices] = {};
+
+static spec_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SPEC_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return SPEC_OK;
+}
+
+spec_status spec_verify_noalloc(const void* target_logits, spec_dtype logits_dtype,
+                                const float* draft_probs, const int32_t* draft_ids,
+                                const int32_t* num_draft, const float* temperature, uint64_t seed,
+                                int B, int K, int V, int32_t* out_ids, int32_t* out_num_accepted,
+                                spec_stream_t stream) {
+    if (!sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
+    if (V % 8 != 0) return SPEC_ERR_UNSUPPORTED;
+    if (make_layout(B, K, V).total > SPEC_NOALLOC_SCRATCH_BYTES) return SPEC_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    const spec_status s = noalloc_scratch(&scratch);
+    if (s != SPEC_OK) return s;
+    return spec_verify(target_logits, logits_dtype, draft_probs, draft_ids, num_draft,
+                       temperature, seed, B, K, V, out_ids, out_num_accepted, scratch,
+                       SPEC_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 spec_status spec_philox_fill(uint64_t seed, const uint32_t* ctrs, int64_t n, uint32_t* out,
                              spec_stream_t stream) {
     if (n < 0 || (n > 0 && (!ctrs || !out))) return SPEC_ERR_INVALID_ARG;
