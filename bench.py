@@ -51,8 +51,8 @@ TILE = 2048  # tokens per row-statistics chunk (one 16-byte partial each)
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=4, help="workload 1..5 (default 4)")
     ap.add_argument("--batch", type=int, default=None, help="leading-B subset (sweep)")
@@ -78,8 +78,13 @@ def measured_peak():
         return PEAK_FALLBACK_GBS, "fallback", {}
 
 
-def source_sha(path):
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+def row_stats_sha():
+    """Digest of the sources k_row_stats is compiled from."""
+    h = hashlib.sha256()
+    for f in ("row_stats.cu", "accept.cuh", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "speculative_decoding_verification_51_gb300", "csrc", f),
+                      "rb").read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload_name: str):
@@ -90,68 +95,102 @@ def profiled_traffic(workload_name: str):
         d = json.load(open(p))
     except Exception:
         return None
-    src = os.path.join(ROOT, "speculative_decoding_verification_51_gb300", "csrc", "row_stats.cu")
-    if d.get("source_sha") != source_sha(src):
+    if d.get("source_sha") != row_stats_sha():
         return None
     e = d.get("workloads", {}).get(workload_name)
     return None if e is None else float(e["dram_bytes_per_launch"])
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """SM clock and clock-event (throttle) reasons sampled through NVML every
+    millisecond during the timed region (falls back to nvidia-smi at 100 ms)."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
-
-    def __enter__(self):
+    def __init__(self, device: torch.device):
+        self.device = device
+        self.samples = []  # (sm_mhz, max_mhz, reason_bits)
+        self.stop = threading.Event()
+        self.nvml = None
+        self.handle = None
+        self.source = None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            props = torch.cuda.get_device_properties(device)
+            uuid = str(getattr(props, "uuid", ""))
+            h = ctypes.c_void_p()
+            ok = False
+            if uuid:
+                ok = nv.nvmlDeviceGetHandleByUUID(f"GPU-{uuid}".encode(), ctypes.byref(h)) == 0
+            if not ok:
+                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+                idx = int(vis.split(",")[device.index or 0]) if vis and vis.split(",")[0].isdigit() \
+                    else (device.index or 0)
+                ok = nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) == 0
+            if not ok:
+                raise OSError("no NVML handle")
+            self.nvml, self.handle, self.ct = nv, h, ctypes
+            self.getreasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.source = "nvml"
+        except Exception:
+            self.nvml = None
+
+    def _poll(self):
+        ct, nv, h = self.ct, self.nvml, self.handle
+        mhz, mx, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        while not self.stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) == 0 and \
+                    nv.nvmlDeviceGetMaxClockInfo(h, 1, ct.byref(mx)) == 0 and \
+                    self.getreasons(h, ct.byref(rs)) == 0:
+                self.samples.append((mhz.value, mx.value, rs.value))
+            time.sleep(0.001)
+
+    def _smi(self):
+        try:
+            proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device.index or 0),
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
         except Exception:
-            self.proc = None
+            return
+        self.source = "nvidia-smi"
+        while not self.stop.is_set():
+            ln = proc.stdout.readline()
+            if not ln:
+                break
+            parts = [x.strip() for x in ln.split(",")]
+            try:
+                self.samples.append((float(parts[0]), float(parts[1]), int(parts[2], 16)))
+            except (ValueError, IndexError):
+                pass
+        proc.terminate()
+
+    def __enter__(self):
+        self.t = threading.Thread(target=self._poll if self.nvml else self._smi, daemon=True)
+        self.t.start()
         return self
 
-    def _read(self):
-        for ln in self.proc.stdout:
-            self.lines.append(ln.strip())
-
     def __exit__(self, *a):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
+        self.stop.set()
+        self.t.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 6:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[2:6]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        if not self.samples:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = set()
+        for _, _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(x[0] for x in self.samples),
+                "sm_max_mhz": max(x[1] for x in self.samples), "reasons": sorted(reasons),
+                "samples": len(self.samples), "source": self.source}
 
 
 def workload_name(cid, B):
@@ -282,7 +321,7 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(dev) as clk:
         for i in range(args.steps):
             flush.fill_((i + 7) & 0xFF)
             evs[i][0].record(stream)
@@ -300,18 +339,20 @@ def main():
     clocks = clk.summary()
 
     # ---- per-kernel durations (same workload, marks between the kernels)
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    n_prof = min(args.steps, 50)
+    nk = binding.N_KERNELS
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(n_prof)]
     for m in marks:
         for e in m:
             e.record(stream)
     torch.cuda.synchronize()
-    for i in range(args.steps):
+    for i in range(n_prof):
         flush.fill_((i + 3) & 0xFF)
         binding.spec_verify_profiled(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
                                      w.temperature, 3000 + i, out_ids, out_nacc, ws, marks[i])
     torch.cuda.synchronize()
-    kern_ms = [statistics.mean(m[k].elapsed_time(m[k + 1]) for m in marks) for k in range(4)]
-    names = ["k_plan", "k_row_stats", "k_accept", "k_sample"]
+    kern_ms = [statistics.mean(m[k].elapsed_time(m[k + 1]) for m in marks) for k in range(nk)]
+    names = list(binding.KERNELS)
 
     # ---- algorithmic bytes
     nacc_cpu = out_nacc.cpu().long()
@@ -374,7 +415,7 @@ def main():
         "kernels_ms": {n: round(t, 5) for n, t in zip(names, kern_ms)},
         "accept_rate": float(nacc_cpu.clamp(min=0).sum()) / max(1, pos),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": 4 * args.steps, "clocks": clocks,
+        "gpu_launches": binding.N_KERNELS * args.steps, "clocks": clocks,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

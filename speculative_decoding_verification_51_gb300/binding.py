@@ -22,6 +22,8 @@ BADBIT = {"num_draft": 1, "temperature": 2, "draft_id": 4, "empty_row": 8, "no_p
           "timeout": 32}
 MODE_BAD, MODE_GREEDY, MODE_RESIDUAL, MODE_BONUS, MODE_FALLBACK = -1, 0, 1, 2, 3
 MAX_K = 31
+KERNELS = ("k_plan", "k_row_stats", "k_sample", "k_emit")  # launch order
+N_KERNELS = len(KERNELS)
 
 _LOCK = threading.Lock()
 _LIB = None
@@ -180,11 +182,13 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
 
 def spec_verify_profiled(target_logits, draft_probs, draft_ids, num_draft, temperature, seed,
                          out_ids, out_num_accepted, workspace, events, stream=None) -> None:
-    """spec_verify with five torch.cuda.Event marks around its four kernels
+    """spec_verify with one torch.cuda.Event mark before each kernel and one after the last
     (events must already have been recorded once, so that they exist)."""
     B, K1, V = target_logits.shape
     dt = SPEC_BF16 if target_logits.dtype == torch.bfloat16 else SPEC_F32
-    handles = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    if len(events) != N_KERNELS + 1:
+        raise ValueError(f"need {N_KERNELS + 1} events")
+    handles = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     with torch.cuda.device(target_logits.device):
         rc = lib().spec_verify_profiled(
             _p(target_logits), dt, _p(draft_probs), _p(draft_ids), _p(num_draft),

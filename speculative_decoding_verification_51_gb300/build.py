@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
-SOURCES = ["plan.cu", "row_stats.cu", "accept.cu", "sample.cu", "api.cu"]
+SOURCES = ["plan.cu", "row_stats.cu", "sample.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
 
@@ -38,9 +38,22 @@ def _inputs() -> list[str]:
             + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
+def extra_flags() -> list[str]:
+    """Extra nvcc flags from SPEC_VERIFY_NVCC_EXTRA (e.g. launch-shape -D overrides)."""
+    return os.environ.get("SPEC_VERIFY_NVCC_EXTRA", "").split()
+
+
+def _stamp() -> str:
+    return lib_path() + ".flags"
+
+
 def up_to_date() -> bool:
     out = lib_path()
-    return os.path.exists(out) and os.path.getmtime(out) >= max(os.path.getmtime(p) for p in _inputs())
+    if not os.path.exists(out) or not os.path.exists(_stamp()):
+        return False
+    if open(_stamp()).read() != " ".join(extra_flags()):
+        return False
+    return os.path.getmtime(out) >= max(os.path.getmtime(p) for p in _inputs())
 
 
 def build(force: bool = False, ptxas_verbose: bool = False) -> str:
@@ -50,7 +63,7 @@ def build(force: bool = False, ptxas_verbose: bool = False) -> str:
         return out
     objdir = os.path.join(BUILD, f"obj_{platform.machine()}")
     os.makedirs(objdir, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    extra = (["-Xptxas", "-v"] if ptxas_verbose else []) + extra_flags()
 
     def compile_one(src: str) -> tuple[str, str]:
         obj = os.path.join(objdir, src.replace(".cu", ".o"))
@@ -68,6 +81,8 @@ def build(force: bool = False, ptxas_verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, out)
+    with open(_stamp(), "w") as f:
+        f.write(" ".join(extra_flags()))
     if ptxas_verbose:
         for (_, log), src in zip(results, SOURCES):
             print(f"== {src}\n{log}")

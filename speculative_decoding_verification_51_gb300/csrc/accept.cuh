@@ -1,0 +1,256 @@
+// accept.cuh -- acceptance of one request by one warp, run inside k_row_stats
+// by the warp that completes the request's last (row, chunk) tile.
+//
+// Lane j owns row j of the request.  Steps (pages cited by title / section):
+//   1. merge the chunk partials of every row j <= n_b into the row's max m_j,
+//      normaliser Z_j = sum_x 2^((l_j(x) - m_j) kappa) and, for greedy rows,
+//      the lowest-index argmax (all partial loads issued before any merge;
+//      float32 throughout: the FP64 pipe of this part is slow);
+//   2. acceptance of draft x_j ("深入推测解码" 保证原始分布 step 3,
+//      "RTP-LLM Speculative Engine" 拒绝采样算法): p = 2^((l_j(x_j) - m_j) kappa)
+//      / Z_j with l_j(x_j) and q_j(x_j) gathered by k_row_stats, u_j = Philox
+//      lane 0 of row j; accept iff p > 0 and (q_j(x_j) == 0 or
+//      u_j <= p / q_j(x_j)), tested exactly as u q <= p in float64; greedy
+//      ("投机采样" 精确匹配): accept iff x_j is the row's argmax;
+//   3. first-reject scan in-warp: a_b = position of the lowest zero of the
+//      ballot of acceptance bits ("投机采样" 第五步: drafts after a rejected
+//      one are discarded);
+//   4. write the accepted prefix and the -1 tail; greedy requests also write
+//      the emitted token (argmax of row a_b); sampling requests are queued for
+//      k_sample (residual at row a_b < n_b, bonus at row a_b == n_b).
+// Values written by other warps during the same kernel (partials, gathered
+// logits) are read through L2 (ld.global.cg), after the caller's fence.
+#pragma once
+
+#include <cfloat>
+#include <climits>
+
+#include "common.cuh"
+
+namespace sv {
+
+namespace {
+
+// (m, z) <- (m, z) (+) (m2, z2): sums of 2^((l - m) kappa) with different maxima.
+__device__ __forceinline__ void merge_sum(float& m, float& z, float m2, float z2, float kappa) {
+    if (m2 > m) {
+        const float tm = m;
+        m = m2;
+        m2 = tm;
+        const float tz = z;
+        z = z2;
+        z2 = tz;
+    }
+    if (m2 != -INFINITY && z2 != 0.f) z = fmaf(z2, exp2f(rebase_arg(m2, m, kappa)), z);
+}
+
+__device__ __forceinline__ void merge_argmax(float& m, int& a, float m2, int a2) {
+    if (m2 > m || (m2 == m && a2 < a)) {
+        m = m2;
+        a = a2;
+    }
+}
+
+}  // namespace
+
+// Request b (valid: k_plan has checked num_draft and temperature); whole warp.
+__device__ __noinline__ void accept_request(const Params& P, int b) {
+    const int lane = threadIdx.x & 31;
+    const int K1 = P.K1;
+    int32_t* out = P.out_ids + (size_t)b * K1;
+    const float NaN = __int_as_float(0x7fc00000);
+
+    auto fail = [&](int flags) {
+        if (lane < K1) out[lane] = -1;
+        if (P.dbg_rows && lane < K1) {
+            float* d = P.dbg_rows + ((size_t)b * K1 + lane) * 4;
+            d[0] = d[1] = d[2] = NaN;
+            d[3] = -1.f;
+        }
+        if (lane == 0) {
+            P.out_nacc[b] = -1;
+            atomicOr(P.status, flags);
+            if (P.dbg_req) {
+                float* d = P.dbg_req + (size_t)b * 4;
+                d[0] = float(MODE_BAD);
+                d[1] = d[2] = d[3] = NaN;
+            }
+        }
+    };
+
+    const int n = P.num_draft[b];
+    const float T = P.temp[b];
+    const bool greedy = (T == 0.f);
+    const float kappa = greedy ? 0.f : kappa_of(T);
+
+    // loads that do not depend on the merge go first
+    const bool draft_lane = lane < n;
+    const int x = draft_lane ? P.ids[(size_t)b * P.K + lane] : -1;
+    float2 g = make_float2(0.f, 0.f);
+    if (draft_lane && !greedy) g = __ldcg(P.gath + (size_t)b * K1 + lane);
+    uint4 rb = make_uint4(0, 0, 0, 0);
+    if (!greedy && lane <= n) rb = row_block(P, b, lane);
+
+    // 1. per-row merge, four rows at a time; lane j keeps row j.  With at most
+    // 128 chunks per row a lane's chunks stay in registers: the row max first
+    // (shuffles), then every chunk rebased onto it once (one ex2 each) and
+    // summed (shuffles); greedy rows take the lowest index attaining the max.
+    float my_m = -INFINITY;
+    int my_amax = INT_MAX;
+    float my_Z = 0.f;
+    const Partial* pb = P.part + (size_t)b * K1 * P.C;
+    constexpr int NPL = 4;  // chunks per lane held in registers
+    if (P.C <= 32 * NPL) {
+        for (int j0 = 0; j0 <= n; j0 += 4) {
+            Partial q[4][NPL];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int i = 0; i < NPL; ++i) {
+                    const int c = lane + 32 * i;
+                    if (j0 + jj <= n && c < P.C) {
+                        const double2 raw = __ldcg(reinterpret_cast<const double2*>(
+                            pb + (size_t)(j0 + jj) * P.C + c));
+                        q[jj][i] = *reinterpret_cast<const Partial*>(&raw);
+                    } else {
+                        q[jj][i].m = -INFINITY;
+                        q[jj][i].amax = INT_MAX;
+                        q[jj][i].z = 0.0;
+                    }
+                }
+#pragma unroll 1
+            for (int jj = 0; jj < 4; ++jj) {
+                if (j0 + jj > n) break;
+                float lm = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < NPL; ++i) lm = fmaxf(lm, q[jj][i].m);
+                const float M = warp_max(lm);
+                int A = INT_MAX;
+                float Z = 0.f;
+                if (greedy) {
+                    int la = INT_MAX;
+#pragma unroll
+                    for (int i = 0; i < NPL; ++i)
+                        if (q[jj][i].m == M) la = min(la, q[jj][i].amax);
+                    A = warp_min_int(la);
+                } else {
+                    float lz = 0.f;
+                    if (M != -INFINITY) {
+#pragma unroll
+                        for (int i = 0; i < NPL; ++i)
+                            if (q[jj][i].m != -INFINITY && q[jj][i].z != 0.0)
+                                lz = fmaf(float(q[jj][i].z), ex2_approx(rebase_arg(q[jj][i].m, M, kappa)), lz);
+                    }
+                    Z = warp_sum_f(lz);
+                }
+                if (lane == j0 + jj) {
+                    my_m = M;
+                    my_amax = A;
+                    my_Z = Z;
+                }
+            }
+        }
+    } else {  // long vocabularies: pairwise merges over the lane's chunks
+        for (int j = 0; j <= n; ++j) {
+            float m = -INFINITY;
+            int am = INT_MAX;
+            float z = 0.f;
+            for (int c = lane; c < P.C; c += 32) {
+                const double2 raw =
+                    __ldcg(reinterpret_cast<const double2*>(pb + (size_t)j * P.C + c));
+                const Partial q = *reinterpret_cast<const Partial*>(&raw);
+                if (greedy)
+                    merge_argmax(m, am, q.m, q.amax);
+                else
+                    merge_sum(m, z, q.m, float(q.z), kappa);
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                const float om = __shfl_xor_sync(0xffffffffu, m, o);
+                if (greedy)
+                    merge_argmax(m, am, om, __shfl_xor_sync(0xffffffffu, am, o));
+                else
+                    merge_sum(m, z, om, __shfl_xor_sync(0xffffffffu, z, o), kappa);
+            }
+            if (lane == j) {
+                my_m = m;
+                my_amax = am;
+                my_Z = z;
+            }
+        }
+    }
+
+    // 2. validation of the draft ids and rows this request uses
+    const unsigned bad_id = __ballot_sync(0xffffffffu, draft_lane && (x < 0 || x >= P.V));
+    const unsigned empty = __ballot_sync(0xffffffffu, !greedy && lane <= n && my_m == -INFINITY);
+    if (bad_id | empty) {
+        fail((bad_id ? int(SPEC_BADBIT_DRAFT_ID) : 0) | (empty ? int(SPEC_BADBIT_EMPTY_ROW) : 0));
+        return;
+    }
+
+    // acceptance of draft `lane`
+    bool acc = false;
+    float p = NaN;
+    float u = NaN;
+    if (draft_lane) {
+        if (greedy) {
+            acc = (x == my_amax);
+        } else {
+            const float lx = g.x, qx = g.y;
+            p = __fdiv_rn(exp2f(weight_arg(lx, my_m, offset_of(my_m, kappa), kappa)), my_Z);
+            u = uniform01(rb.x);
+            // u <= p / q  <=>  u q <= p (q > 0); the product of two floats is
+            // exact in double, so the comparison takes no rounding
+            acc = (p > 0.f) && (qx == 0.f || double(u) * double(qx) <= double(p));
+        }
+    }
+
+    // 3. first rejection
+    const unsigned accm = __ballot_sync(0xffffffffu, acc);
+    const int a = min(n, __ffs(~accm) - 1);
+
+    // 4. outputs
+    if (lane < a)
+        out[lane] = x;
+    else if (lane > a && lane < K1)
+        out[lane] = -1;
+    if (greedy && lane == a) out[a] = my_amax;
+    if (lane == 0) P.out_nacc[b] = a;
+    if (!greedy && lane == a) {
+        ReqRec r;
+        r.mode = a < n ? MODE_RESIDUAL : MODE_BONUS;
+        r.erow = a;
+        r.m = my_m;
+        r.kappa = kappa;
+        r.Z = double(my_Z);
+        r.u2 = uniform01(rb.y);
+        r.b = b;
+        if (a < n) {
+            const int i = atomicAdd(&P.hdr[HDR_NRES], 1);
+            P.res_rec[i] = r;
+        } else {
+            const int i = atomicAdd(&P.hdr[HDR_NBONUS], 1);
+            P.bonus_rec[i] = r;
+        }
+    }
+    if (P.dbg_rows && lane < K1) {
+        float* d = P.dbg_rows + ((size_t)b * K1 + lane) * 4;
+        if (draft_lane) {
+            d[0] = greedy ? NaN : p;
+            d[1] = greedy ? NaN : u;
+            d[2] = greedy ? NaN : float(my_Z);
+            d[3] = acc ? 1.f : 0.f;
+        } else {
+            d[0] = d[1] = d[2] = NaN;
+            d[3] = -1.f;
+        }
+    }
+    if (P.dbg_req && greedy && lane == 0) {
+        float* d = P.dbg_req + (size_t)b * 4;
+        d[0] = float(MODE_GREEDY);
+        d[1] = float(a);
+        d[2] = d[3] = NaN;
+    }
+}
+
+}  // namespace sv

@@ -16,7 +16,8 @@ struct DeviceInfo {
     int sms = 0;
     int stats_blocks_bf16 = 0;  // resident k_row_stats CTAs per SM
     int stats_blocks_f32 = 0;
-    int sample_blocks = 0;
+    int sample_blocks_bf16 = 0;  // resident k_sample CTAs per SM
+    int sample_blocks_f32 = 0;
 };
 
 std::mutex g_mu;
@@ -24,6 +25,10 @@ DeviceInfo g_dev[kMaxDevices];
 
 constexpr size_t stats_smem(int dtype) {
     return size_t(STATS_WARPS) * STATS_STAGES * TILE * (dtype == SPEC_BF16 ? 2 : 4);
+}
+// two stages per warp of (logits chunk + draft-probability chunk)
+constexpr size_t sample_smem(int dtype) {
+    return size_t(SAMPLE_WARPS) * 2 * TILE * ((dtype == SPEC_BF16 ? 2 : 4) + 4);
 }
 
 // Per-device launch facts, computed once per device (thread-safe).
@@ -38,7 +43,15 @@ spec_status device_info(DeviceInfo& out) {
         if (cudaFuncSetAttribute(k_row_stats_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(stats_smem(SPEC_BF16))) != cudaSuccess ||
             cudaFuncSetAttribute(k_row_stats_f32, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(stats_smem(SPEC_F32))) != cudaSuccess)
+                                 int(stats_smem(SPEC_F32))) != cudaSuccess ||
+            cudaFuncSetAttribute(k_sample_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sample_smem(SPEC_BF16))) != cudaSuccess ||
+            cudaFuncSetAttribute(k_sample_f32, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sample_smem(SPEC_F32))) != cudaSuccess ||
+            cudaFuncSetAttribute(k_emit_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sample_smem(SPEC_BF16) / 2)) != cudaSuccess ||
+            cudaFuncSetAttribute(k_emit_f32, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sample_smem(SPEC_F32) / 2)) != cudaSuccess)
             return SPEC_ERR_CUDA;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.stats_blocks_bf16,
                                                           k_row_stats_bf16, STATS_WARPS * 32,
@@ -46,20 +59,37 @@ spec_status device_info(DeviceInfo& out) {
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.stats_blocks_f32,
                                                           k_row_stats_f32, STATS_WARPS * 32,
                                                           stats_smem(SPEC_F32)) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sample_blocks, k_sample_bf16,
-                                                          SAMPLE_THREADS, 0) != cudaSuccess)
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sample_blocks_bf16, k_sample_bf16,
+                                                          SAMPLE_WARPS * 32,
+                                                          sample_smem(SPEC_BF16)) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sample_blocks_f32, k_sample_f32,
+                                                          SAMPLE_WARPS * 32,
+                                                          sample_smem(SPEC_F32)) != cudaSuccess)
             return SPEC_ERR_CUDA;
         d.stats_blocks_bf16 = d.stats_blocks_bf16 < 1 ? 1 : d.stats_blocks_bf16;
         d.stats_blocks_f32 = d.stats_blocks_f32 < 1 ? 1 : d.stats_blocks_f32;
-        d.sample_blocks = d.sample_blocks < 1 ? 1 : (d.sample_blocks > 4 ? 4 : d.sample_blocks);
+        d.sample_blocks_bf16 = d.sample_blocks_bf16 < 1 ? 1 : d.sample_blocks_bf16;
+        d.sample_blocks_f32 = d.sample_blocks_f32 < 1 ? 1 : d.sample_blocks_f32;
         d.ready = true;
     }
     out = d;
     return SPEC_OK;
 }
 
+// Programmatic dependent launch lets a kernel's launch and prologue overlap
+// its predecessor's tail; every kernel still executes griddepcontrol.wait
+// before it reads its predecessor's output, so either launch mode is correct.
+// Measured on GB300 with the four kernels of a call: plain stream order was
+// faster than programmatic dependent launch, so it is off unless -DSV_PDL.
+#ifdef SV_PDL
+constexpr bool kUsePdl = true;
+#else
+constexpr bool kUsePdl = false;
+#endif
+
 cudaError_t launch(void (*kern)(Params), unsigned grid, unsigned block, size_t smem,
                    cudaStream_t st, bool pdl, const Params& P) {
+    pdl = pdl && kUsePdl;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
@@ -123,11 +153,11 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     P.rowlist = at<int>(workspace, L.rowlist);
     P.req_flags = at<int>(workspace, L.req_flags);
     P.part = at<Partial>(workspace, L.part);
-    P.reqs = at<ReqRec>(workspace, L.reqs);
-    P.res_list = at<int>(workspace, L.res_list);
-    P.bonus_list = at<int>(workspace, L.bonus_list);
-    P.res_cnt = at<int>(workspace, L.res_cnt);
-    P.rsum = at<double>(workspace, L.rsum);
+    P.res_rec = at<ReqRec>(workspace, L.res_rec);
+    P.bonus_rec = at<ReqRec>(workspace, L.bonus_rec);
+    P.rsum = at<float>(workspace, L.rsum);
+    P.gath = at<float2>(workspace, L.gath);
+    P.cnt = at<int>(workspace, L.cnt);
     P.seed = seed;
     P.req_off = request_offset;
     P.dtype = logits_dtype;
@@ -136,7 +166,6 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     P.K1 = K + 1;
     P.V = V;
     P.C = (V + TILE - 1) / TILE;
-    P.C2 = (V + CH2 - 1) / CH2;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const bool bf16 = logits_dtype == SPEC_BF16;
@@ -144,10 +173,10 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     long long g1 = (long long)dev.sms * (bf16 ? dev.stats_blocks_bf16 : dev.stats_blocks_f32);
     const long long need1 = (max_tiles + STATS_WARPS - 1) / STATS_WARPS;
     if (g1 > need1) g1 = need1;
-    const unsigned g2 = unsigned((B + ACCEPT_WARPS - 1) / ACCEPT_WARPS);
-    long long g3 = (long long)dev.sms * dev.sample_blocks;
-    const long long need3 = (long long)B * P.C2 + B;
+    long long g3 = (long long)dev.sms * (bf16 ? dev.sample_blocks_bf16 : dev.sample_blocks_f32);
+    const long long need3 = ((long long)B * P.C + SAMPLE_WARPS - 1) / SAMPLE_WARPS;
     if (g3 > need3) g3 = need3;
+    const unsigned g4 = unsigned((B + SAMPLE_WARPS - 1) / SAMPLE_WARPS);  // a warp per draw
 
     // events (profiling only) are recorded before each kernel and after the last
     auto mark = [&](int i) { return events ? cudaEventRecord(events[i], st) : cudaSuccess; };
@@ -158,11 +187,13 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
         e = launch(bf16 ? k_row_stats_bf16 : k_row_stats_f32, unsigned(g1),
                    STATS_WARPS * 32, stats_smem(logits_dtype), st, true, P);
     if (e == cudaSuccess) e = mark(2);
-    if (e == cudaSuccess) e = launch(k_accept, g2, ACCEPT_WARPS * 32, 0, st, true, P);
+    if (e == cudaSuccess)
+        e = launch(bf16 ? k_sample_bf16 : k_sample_f32, unsigned(g3), SAMPLE_WARPS * 32,
+                   sample_smem(logits_dtype), st, true, P);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess)
-        e = launch(bf16 ? k_sample_bf16 : k_sample_f32, unsigned(g3), SAMPLE_THREADS,
-                   0, st, true, P);
+        e = launch(bf16 ? k_emit_bf16 : k_emit_f32, g4, SAMPLE_WARPS * 32,
+                   sample_smem(logits_dtype) / 2, st, true, P);
     if (e == cudaSuccess) e = mark(4);
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

@@ -1,18 +1,22 @@
 // common.cuh -- shared definitions of the spec_verify kernels (sm_103a).
 //
 // Pipeline of one spec_verify call (all on the caller's stream):
-//   k_plan       1 CTA: validate num_draft / temperature, compact the rows
-//                every request needs (j = 0..n_b) into a row list.
+//   k_plan       1 CTA: validate num_draft / temperature (bad requests get
+//                their -1 outputs here), compact the rows every request needs
+//                (j = 0..n_b) into a row list, zero the counters.
 //   k_row_stats  persistent, one independent bulk-copy pipeline per warp: for
 //                every (valid row, 2048-token chunk) the chunk max, the sum of
 //                exp2((l - max) * log2(e) / T) and (greedy rows) the argmax.
-//   k_accept     one warp per request: merge the chunk partials into per-row
-//                (max, Z, argmax), gather l(x_j) and q(x_j), draw Philox
-//                uniforms, acceptance bits, first-reject scan (ballot), write
-//                the accepted prefix; queue sampling requests.
-//   k_sample     persistent: residual chunk sums over the first rejected row,
-//                then (last CTA per request) the two-level inverse CDF; bonus
-//                tokens by the same inverse CDF over the row-stat partials.
+//                The warp that finishes the last tile of a request then runs
+//                its acceptance (accept.cuh): merge the chunk partials into
+//                per-row (max, Z, argmax), take l(x_j) and q(x_j), draw
+//                Philox uniforms, acceptance bits, first-reject scan (ballot),
+//                write the accepted prefix, queue sampling requests.
+//   k_sample     persistent, warp units: the residual chunk masses of the
+//                first rejected row of every rejecting request (streaming).
+//   k_emit       one warp per draw: residual tokens (two-level inverse CDF
+//                over the chunk masses) and bonus tokens (over the row-stat
+//                partials).
 // Kernels after k_plan are launched with programmatic dependent launch; each
 // CTA executes griddepcontrol.wait before it touches its predecessor's output.
 #pragma once
@@ -26,12 +30,21 @@ namespace sv {
 
 // ---------------------------------------------------------------- sizes
 
-constexpr int TILE = 2048;           // tokens per row-stat chunk (one warp tile)
-constexpr int STATS_WARPS = 8;       // warps per k_row_stats CTA
-constexpr int STATS_STAGES = 3;      // bulk-copy stages per warp
-constexpr int CH2 = 8192;            // tokens per residual chunk (one CTA unit)
-constexpr int SAMPLE_THREADS = 256;  // k_sample CTA
-constexpr int ACCEPT_WARPS = 8;      // requests per k_accept CTA
+// Launch-shape parameters (overridable at build time for tuning sweeps).
+#ifndef SV_STATS_WARPS
+#define SV_STATS_WARPS 8
+#endif
+#ifndef SV_STATS_STAGES
+#define SV_STATS_STAGES 3
+#endif
+#ifndef SV_SAMPLE_WARPS
+#define SV_SAMPLE_WARPS 4
+#endif
+
+constexpr int TILE = 2048;                    // tokens per row-stat chunk (one warp tile)
+constexpr int STATS_WARPS = SV_STATS_WARPS;   // warps per k_row_stats CTA
+constexpr int STATS_STAGES = SV_STATS_STAGES; // bulk-copy stages per warp
+constexpr int SAMPLE_WARPS = SV_SAMPLE_WARPS;  // warps per k_sample CTA (2 staging buffers each)
 constexpr int PLAN_THREADS = 1024;
 
 enum { HDR_ROWS = 0, HDR_NRES = 1, HDR_NBONUS = 2, HDR_STATUS = 3, HDR_INTS = 64 };
@@ -44,7 +57,7 @@ struct __align__(16) Partial {
     double z;    // sampling rows: sum exp2((l - m) * kappa) over the chunk
 };
 
-// Per request decision written by k_accept for sampling requests.
+// A queued sampling draw, written by k_accept.
 struct __align__(16) ReqRec {
     int mode;     // MODE_*
     int erow;     // row the emitted token is drawn from
@@ -71,40 +84,38 @@ struct Params {
     int* rowlist;     // [B*(K+1)] slot = b*(K+1)+j of each compacted row
     int* req_flags;   // [B] bad bits found by k_plan
     Partial* part;    // [B*(K+1)*C]
-    ReqRec* reqs;     // [B]
-    int* res_list;    // [B]
-    int* bonus_list;  // [B]
-    int* res_cnt;     // [B] finished residual chunks per queued request
-    double* rsum;     // [B*C2] residual chunk sums
+    ReqRec* res_rec;    // [B] queued residual draws (queue order)
+    ReqRec* bonus_rec;  // [B] queued bonus draws (queue order)
+    float* rsum;      // [B*C] residual chunk sums (TILE-token chunks)
+    float2* gath;     // [B*(K+1)] {l_j(x_j), q_j(x_j)} gathered by k_row_stats
+    int* cnt;         // [B] (row, chunk) tiles of each request finished so far
     uint64_t seed;
     uint32_t req_off;
     int dtype;  // SPEC_F32 / SPEC_BF16
     int B, K, K1, V;
-    int C;   // ceil(V / TILE)
-    int C2;  // ceil(V / CH2)
+    int C;   // ceil(V / TILE): chunks per row
 };
 
 // Workspace layout (byte offsets, each section 256-byte aligned).
 struct Layout {
-    size_t hdr, rowlist, req_flags, part, reqs, res_list, bonus_list, res_cnt, rsum, total;
+    size_t hdr, rowlist, req_flags, part, res_rec, bonus_rec, rsum, gath, cnt, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 inline Layout make_layout(int B, int K, int V) {
     Layout L;
-    const size_t K1 = size_t(K) + 1, C = (size_t(V) + TILE - 1) / TILE,
-                 C2 = (size_t(V) + CH2 - 1) / CH2;
+    const size_t K1 = size_t(K) + 1, C = (size_t(V) + TILE - 1) / TILE;
     size_t o = 0;
     L.hdr = o;        o = align256(o + HDR_INTS * sizeof(int));
     L.rowlist = o;    o = align256(o + size_t(B) * K1 * sizeof(int));
     L.req_flags = o;  o = align256(o + size_t(B) * sizeof(int));
     L.part = o;       o = align256(o + size_t(B) * K1 * C * sizeof(Partial));
-    L.reqs = o;       o = align256(o + size_t(B) * sizeof(ReqRec));
-    L.res_list = o;   o = align256(o + size_t(B) * sizeof(int));
-    L.bonus_list = o; o = align256(o + size_t(B) * sizeof(int));
-    L.res_cnt = o;    o = align256(o + size_t(B) * sizeof(int));
-    L.rsum = o;       o = align256(o + size_t(B) * C2 * sizeof(double));
+    L.res_rec = o;    o = align256(o + size_t(B) * sizeof(ReqRec));
+    L.bonus_rec = o;  o = align256(o + size_t(B) * sizeof(ReqRec));
+    L.rsum = o;       o = align256(o + size_t(B) * C * sizeof(float));
+    L.gath = o;       o = align256(o + size_t(B) * K1 * sizeof(float2));
+    L.cnt = o;        o = align256(o + size_t(B) * sizeof(int));
     L.total = o;
     return L;
 }
@@ -185,6 +196,32 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Token weights are w(x) = 2^((l(x) - m) kappa) for a reference maximum m.
+// With the offset c = RN(m * kappa) the exponent is one FFMA, l * kappa - c
+// (the product is exact inside the FMA).  Every kernel that computes weights
+// of the same tokens uses the same m, hence the same c, so the rounding of c
+// is a common factor that cancels in every normalised quantity.  When c is
+// not finite (absurdly small T) the two-operation form (l - m) * kappa is
+// used instead; both forms give 2^0 at l == m and 0 far below it.
+__device__ __forceinline__ float offset_of(float m, float kappa) { return __fmul_rn(m, kappa); }
+__device__ __forceinline__ float weight_arg(float l, float m, float c, float kappa) {
+    return isfinite(c) ? fmaf(l, kappa, -c) : __fmul_rn(__fsub_rn(l, m), kappa);
+}
+// Exponent of the factor 2^((m_c - m) kappa) that rebases weights computed
+// against m_c onto m, consistent with weight_arg.
+__device__ __forceinline__ float rebase_arg(float m_c, float m, float kappa) {
+    const float cc = offset_of(m_c, kappa), cm = offset_of(m, kappa);
+    return (isfinite(cc) && isfinite(cm)) ? __fsub_rn(cc, cm)
+                                          : __fmul_rn(__fsub_rn(m_c, m), kappa);
+}
+
+// Packed bf16x2 maximum (NaN operands lose).
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -237,6 +274,11 @@ __device__ __forceinline__ float warp_max(float v) {
     for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
 __device__ __forceinline__ double warp_sum(double v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -257,9 +299,11 @@ __device__ __forceinline__ int warp_max_int(int v) {
 __global__ void k_plan(Params P);
 __global__ void k_row_stats_f32(Params P);
 __global__ void k_row_stats_bf16(Params P);
-__global__ void k_accept(Params P);
 __global__ void k_sample_f32(Params P);
 __global__ void k_sample_bf16(Params P);
+__global__ void k_emit_f32(Params P);
+__global__ void k_emit_bf16(Params P);
+
 __global__ void k_philox_fill(uint64_t seed, const uint32_t* ctrs, int64_t n, uint32_t* out);
 
 }  // namespace sv

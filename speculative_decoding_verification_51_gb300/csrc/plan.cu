@@ -36,7 +36,24 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_plan(Params P) {
             if (!flags && T > 0.f && n > 0 && P.probs == nullptr) flags |= SPEC_BADBIT_NO_PROBS;
             rows = flags ? 0 : n + 1;
             P.req_flags[b] = flags;
+            P.cnt[b] = 0;
             flags_any |= flags;
+            if (flags) {  // no row of a bad request is read: its outputs are final here
+                for (int j = 0; j < P.K1; ++j) P.out_ids[(size_t)b * P.K1 + j] = -1;
+                P.out_nacc[b] = -1;
+                const float NaN = __int_as_float(0x7fc00000);
+                if (P.dbg_rows)
+                    for (int j = 0; j < P.K1; ++j) {
+                        float* d = P.dbg_rows + ((size_t)b * P.K1 + j) * 4;
+                        d[0] = d[1] = d[2] = NaN;
+                        d[3] = -1.f;
+                    }
+                if (P.dbg_req) {
+                    float* d = P.dbg_req + (size_t)b * 4;
+                    d[0] = float(MODE_BAD);
+                    d[1] = d[2] = d[3] = NaN;
+                }
+            }
         }
         // block-wide exclusive scan of the row counts
         int incl = rows;

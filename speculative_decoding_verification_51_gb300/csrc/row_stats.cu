@@ -12,13 +12,26 @@
 // (row, chunk) tiles are divided into equal contiguous ranges, one per warp.
 // Each warp runs its own STATS_STAGES-deep pipeline: lane 0 issues a 1-D bulk
 // copy (cp.async.bulk, completion on a per-stage mbarrier) for the tile
-// STATS_STAGES ahead while the warp reduces the current tile from shared
-// memory with 16-byte loads: chunk max by warp shuffles, then the sum of
-// exp2((l - max) * log2(e)/T) per lane in float32, summed across lanes in
-// float64.  No block-wide barrier is used.  Output: one Partial per tile.
+// STATS_STAGES ahead while the warp reduces the current tile out of shared
+// memory (16-byte loads, 64 tokens per lane):
+//   sampling rows: chunk max by a packed bf16x2 max tree and shuffles, then
+//     the sum of 2^(l * kappa - c) with c = RN(max * kappa) (one FFMA and one
+//     ex2 per token, pairwise float32 sums, shuffles);
+//   greedy rows: chunk max, then the lowest index attaining it.
+// While the tile holding the draft token x_j of a row is in shared memory its
+// logit is copied out, and q_j(x_j) is fetched, for the acceptance test.
+// No block-wide barrier and no float64 arithmetic (the FP64 pipe of this part
+// is a small fraction of its FP32 rate).  Output: one Partial per tile.
+//
+// Completion: each warp adds the number of tiles it finished for a request to
+// the request's counter (one atomic per contiguous run of that request's
+// tiles, after a threadfence); the warp whose addition completes the count
+// (n_b + 1) * C runs the request's acceptance (accept_request) at once.
+// Nothing ever waits for another warp.
 #include <cfloat>
 #include <climits>
 
+#include "accept.cuh"
 #include "common.cuh"
 
 namespace sv {
@@ -47,6 +60,63 @@ __device__ __forceinline__ void unpack(const uint4& v, float (&f)[Tile<DT>::EPV]
     }
 }
 
+// Maximum of a lane's VPL vectors (tree; packed bf16x2 for bf16).
+template <int DT>
+__device__ __forceinline__ float lane_max(const uint4 (&d)[Tile<DT>::VPL]) {
+    constexpr int VPL = Tile<DT>::VPL;
+    if constexpr (DT == SPEC_BF16) {
+        uint32_t w[VPL];
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) w[k] = bmax2(bmax2(d[k].x, d[k].y), bmax2(d[k].z, d[k].w));
+#pragma unroll
+        for (int h = VPL / 2; h; h >>= 1)
+#pragma unroll
+            for (int k = 0; k < h; ++k) w[k] = bmax2(w[k], w[k + h]);
+        return fmaxf(bf16_lo(w[0]), bf16_hi(w[0]));
+    } else {
+        float w[VPL];
+#pragma unroll
+        for (int k = 0; k < VPL; ++k)
+            w[k] = fmaxf(fmaxf(__uint_as_float(d[k].x), __uint_as_float(d[k].y)),
+                         fmaxf(__uint_as_float(d[k].z), __uint_as_float(d[k].w)));
+#pragma unroll
+        for (int h = VPL / 2; h; h >>= 1)
+#pragma unroll
+            for (int k = 0; k < h; ++k) w[k] = fmaxf(w[k], w[k + h]);
+        return w[0];
+    }
+}
+
+// Per-row facts a warp needs while it streams the row's chunks.
+struct RowCtx {
+    int slot;      // b * (K+1) + j
+    int b;         // request
+    int n;         // num_draft[b]
+    bool greedy;
+    float kappa;   // log2(e) / T
+    int xj;        // draft token of the row (-1: none, or out of range)
+    int xchunk;    // chunk holding xj (-1: none)
+};
+
+__device__ __forceinline__ RowCtx row_ctx(const Params& P, long long r) {
+    RowCtx rc;
+    rc.slot = P.rowlist[r];
+    const int b = rc.slot / P.K1, j = rc.slot - b * P.K1;
+    rc.b = b;
+    rc.n = P.num_draft[b];
+    const float T = P.temp[b];
+    rc.greedy = (T == 0.f);
+    rc.kappa = rc.greedy ? 0.f : kappa_of(T);
+    int x = -1;
+    if (!rc.greedy && j < rc.n) {
+        x = P.ids[(size_t)b * P.K + j];
+        if (x < 0 || x >= P.V) x = -1;  // reported by k_accept
+    }
+    rc.xj = x;
+    rc.xchunk = x >= 0 ? x / TILE : -1;
+    return rc;
+}
+
 }  // namespace
 
 template <int DT>
@@ -73,150 +143,194 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
     const long long w = (long long)blockIdx.x * STATS_WARPS + warp;
     const long long t0 = T * w / W, t1 = T * (w + 1) / W;
     if (t0 >= t1) return;
+    const long long r0 = t0 / P.C;
+    const int c0 = int(t0 - r0 * P.C);
+    const long long n_tiles = t1 - t0;
 
-    // lane 0: issue tile t into stage s (row cache: consecutive tiles share rows)
-    long long prow = -1;
-    int pslot = 0;
-    auto issue = [&](long long t, int s) {
-        const long long r = t / P.C;
-        const int c = int(t - r * P.C);
-        if (r != prow) {
-            prow = r;
-            pslot = P.rowlist[r];
-        }
-        const int nel = min(TILE, P.V - c * TILE);
+    // producer (lane 0): next tile to issue, as (row, chunk), and its row's slot
+    long long pr = r0;
+    int pc = c0;
+    int pslot = lane == 0 ? P.rowlist[r0] : 0;
+    auto issue = [&](int s) {
+        const int nel = min(TILE, P.V - pc * TILE);
         const uint32_t bytes = uint32_t(nel) * TL::ESZ;
         const char* src = reinterpret_cast<const char*>(P.logits) +
-                          ((size_t)pslot * P.V + (size_t)c * TILE) * TL::ESZ;
+                          ((size_t)pslot * P.V + (size_t)pc * TILE) * TL::ESZ;
         mbar_arrive_expect_tx(&bars[warp][s], bytes);
         bulk_g2s(buf + s * TL::BYTES, src, bytes, &bars[warp][s]);
+        if (++pc == P.C) {
+            pc = 0;
+            if (++pr < R) pslot = P.rowlist[pr];
+        }
     };
     if (lane == 0) {
-        for (int k = 0; k < STATS_STAGES && t0 + k < t1; ++k) issue(t0 + k, k);
+        for (int k = 0; k < STATS_STAGES && k < n_tiles; ++k) issue(k);
     }
 
-    long long crow = -1;
-    int slot = 0;
-    bool greedy = false;
-    float kappa = 0.f;
-    long long t = t0;
-    bool timed_out = false;
-    for (; t < t1; ++t) {
-        const long long i = t - t0;
-        const int s = int(i % STATS_STAGES);
-        const uint32_t parity = uint32_t((i / STATS_STAGES) & 1);
-        const long long r = t / P.C;
-        const int c = int(t - r * P.C);
-        if (r != crow) {
-            crow = r;
-            slot = P.rowlist[r];
-            const float Tb = P.temp[slot / P.K1];
-            greedy = (Tb == 0.f);
-            kappa = greedy ? 0.f : kappa_of(Tb);
+    // consumer state
+    long long cr = r0;
+    int cc = c0;
+    RowCtx rc = row_ctx(P, cr);
+    float qx = 0.f;  // q_j(x_j), fetched at row start by the warp that owns x_j's tile
+    auto prefetch_q = [&]() {
+        const long long t_x = cr * P.C + rc.xchunk;
+        if (rc.xj >= 0 && t_x >= t0 && t_x < t1 && lane == 0) {
+            const int b = rc.slot / P.K1, j = rc.slot - b * P.K1;
+            qx = __ldg(P.probs + ((size_t)b * P.K + j) * P.V + rc.xj);
         }
-        const int nvec = min(TILE, P.V - c * TILE) / EPV;
+    };
+    prefetch_q();
+
+    // the run of consecutive tiles of one request that this warp has finished
+    int seg_b = rc.b, seg_n = rc.n, seg_tiles = 0;
+    auto flush = [&]() {
+        int last = 0;
+        if (lane == 0 && seg_tiles > 0) {
+            __threadfence();  // this warp's partials before its count
+            const int total = (seg_n + 1) * P.C;
+            last = atomicAdd(&P.cnt[seg_b], seg_tiles) + seg_tiles == total;
+        }
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+            __threadfence();  // every other warp's partials after the count
+            accept_request(P, seg_b);
+        }
+        seg_tiles = 0;
+    };
+
+    long long i = 0;
+    int s = 0;            // stage of tile i
+    uint32_t parity = 0;  // phase of that stage's barrier
+    bool timed_out = false;
+    for (; i < n_tiles; ++i) {
+        const int nvec = min(TILE, P.V - cc * TILE) / EPV;
 
         const bool landed = mbar_wait_bounded(&bars[warp][s], parity);
         if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform exit
             timed_out = true;
             break;
         }
-        const uint4* v4 = reinterpret_cast<const uint4*>(buf + s * TL::BYTES);
+        const uint8_t* stage = buf + s * TL::BYTES;
+        const uint4* v4 = reinterpret_cast<const uint4*>(stage);
         uint4 d[VPL];
+        if (nvec == TILE / EPV) {  // full tile
 #pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-            const int v = k * 32 + lane;
-            d[k] = v < nvec ? v4[v]
-                            : make_uint4(TL::NEG_INF_WORD, TL::NEG_INF_WORD, TL::NEG_INF_WORD,
-                                         TL::NEG_INF_WORD);
-        }
-        __syncwarp();  // every lane holds its share: the stage can be refilled
-        if (lane == 0 && t + STATS_STAGES < t1) {
-            fence_proxy_async_smem();
-            issue(t + STATS_STAGES, s);
-        }
-
-        const int tok0 = c * TILE;
-        Partial out;
-        if (greedy) {
-            // lowest index of the maximum: lanes visit their tokens in increasing order
-            float best = -INFINITY;
-            int bidx = INT_MAX;
+            for (int k = 0; k < VPL; ++k) d[k] = v4[k * 32 + lane];
+        } else {                   // the row's ragged last chunk: pad with -inf
 #pragma unroll
             for (int k = 0; k < VPL; ++k) {
+                const int v = k * 32 + lane;
+                d[k] = v < nvec ? v4[v]
+                                : make_uint4(TL::NEG_INF_WORD, TL::NEG_INF_WORD,
+                                             TL::NEG_INF_WORD, TL::NEG_INF_WORD);
+            }
+        }
+        const bool has_x = (cc == rc.xchunk);
+        float lx = 0.f;
+        if (has_x && lane == 0) {
+            const int e = rc.xj - cc * TILE;
+            if constexpr (DT == SPEC_BF16)
+                lx = __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(stage)[e]) << 16);
+            else
+                lx = reinterpret_cast<const float*>(stage)[e];
+        }
+        __syncwarp();  // every lane holds its share: the stage can be refilled
+        if (lane == 0 && i + STATS_STAGES < n_tiles) {  // tile i + STAGES reuses stage s
+            fence_proxy_async_smem();
+            issue(s);
+        }
+
+        const int tok0 = cc * TILE;
+        const float m = warp_max(lane_max<DT>(d));
+        Partial out;
+        out.m = m;
+        if (rc.greedy) {
+            // lowest index attaining m: visiting tokens from high to low index
+            // leaves the lowest hit
+            int bidx = INT_MAX;
+#pragma unroll
+            for (int k = VPL - 1; k >= 0; --k) {
                 if (k * 32 + lane < nvec) {
                     float f[EPV];
                     unpack<DT>(d[k], f);
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        if (f[e] > best || bidx == INT_MAX) {
-                            best = f[e];
-                            bidx = tok0 + (k * 32 + lane) * EPV + e;
-                        }
-                    }
+                    for (int e = EPV - 1; e >= 0; --e)
+                        if (f[e] == m) bidx = tok0 + (k * 32 + lane) * EPV + e;
                 }
             }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) {
-                const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
-                if (ob > best || (ob == best && oi < bidx)) {
-                    best = ob;
-                    bidx = oi;
-                }
-            }
-            out.m = best;
-            out.amax = bidx;
+            out.amax = warp_min_int(bidx);
             out.z = 0.0;
         } else {
-            float lmax = -INFINITY;
-#pragma unroll
-            for (int k = 0; k < VPL; ++k) {
-                float f[EPV];
-                unpack<DT>(d[k], f);
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) lmax = fmaxf(lmax, f[e]);
-            }
-            const float m = warp_max(lmax);
-            double z = 0.0;
+            float z = 0.f;
             if (m != -INFINITY) {
+                const float c = offset_of(m, rc.kappa);
                 float zs[VPL];
+                if (isfinite(c)) {  // one FFMA + ex2 per token
 #pragma unroll
-                for (int k = 0; k < VPL; ++k) {
-                    float f[EPV];
-                    unpack<DT>(d[k], f);
-                    float e4[EPV];
+                    for (int k = 0; k < VPL; ++k) {
+                        float f[EPV];
+                        unpack<DT>(d[k], f);
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e)
-                        e4[e] = ex2_approx(__fmul_rn(__fsub_rn(f[e], m), kappa));
-                    // pairwise within the vector
+                        for (int e = 0; e < EPV; ++e) f[e] = ex2_approx(fmaf(f[e], rc.kappa, -c));
 #pragma unroll
-                    for (int h = EPV / 2; h; h >>= 1)
+                        for (int h = EPV / 2; h; h >>= 1)
 #pragma unroll
-                        for (int e = 0; e < h; ++e) e4[e] = __fadd_rn(e4[e], e4[e + h]);
-                    zs[k] = e4[0];
+                            for (int e = 0; e < h; ++e) f[e] = __fadd_rn(f[e], f[e + h]);
+                        zs[k] = f[0];
+                    }
+                } else {  // offset overflows (absurdly small T): (l - m) * kappa
+#pragma unroll
+                    for (int k = 0; k < VPL; ++k) {
+                        float f[EPV];
+                        unpack<DT>(d[k], f);
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e)
+                            f[e] = ex2_approx(__fmul_rn(__fsub_rn(f[e], m), rc.kappa));
+#pragma unroll
+                        for (int h = EPV / 2; h; h >>= 1)
+#pragma unroll
+                            for (int e = 0; e < h; ++e) f[e] = __fadd_rn(f[e], f[e + h]);
+                        zs[k] = f[0];
+                    }
                 }
 #pragma unroll
                 for (int h = VPL / 2; h; h >>= 1)
 #pragma unroll
                     for (int k = 0; k < h; ++k) zs[k] = __fadd_rn(zs[k], zs[k + h]);
-                z = warp_sum(double(zs[0]));
+                z = warp_sum_f(zs[0]);
             }
-            out.m = m;
             out.amax = -1;
-            out.z = z;
+            out.z = double(z);
         }
-        if (lane == 0) P.part[(size_t)slot * P.C + c] = out;
+        if (lane == 0) {
+            P.part[(size_t)rc.slot * P.C + cc] = out;
+            if (has_x) P.gath[rc.slot] = make_float2(lx, qx);
+        }
+        ++seg_tiles;
+        if (++cc == P.C) {
+            cc = 0;
+            if (++cr < R && i + 1 < n_tiles) {
+                rc = row_ctx(P, cr);
+                prefetch_q();
+                if (rc.b != seg_b) {  // the warp moves on to the next request
+                    flush();
+                    seg_b = rc.b;
+                    seg_n = rc.n;
+                }
+            }
+        }
+        if (++s == STATS_STAGES) {
+            s = 0;
+            parity ^= 1u;
+        }
     }
 
+    if (!timed_out) flush();
     if (timed_out) {
         if (lane == 0) atomicOr(P.status, int(SPEC_BADBIT_TIMEOUT));
         // let the copies still in flight land before the CTA's shared memory is released
-        for (long long u = t; u < t1 && u < t + STATS_STAGES; ++u) {
-            const long long i = u - t0;
-            mbar_wait_bounded(&bars[warp][int(i % STATS_STAGES)],
-                              uint32_t((i / STATS_STAGES) & 1), 100000000ull);
-        }
+        for (long long u = i; u < n_tiles && u < i + STATS_STAGES; ++u)
+            mbar_wait_bounded(&bars[warp][int(u % STATS_STAGES)], uint32_t((u / STATS_STAGES) & 1),
+                              100000000ull);
     }
 }
 

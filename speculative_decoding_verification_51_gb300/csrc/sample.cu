@@ -7,17 +7,24 @@
 // uniform u' (Philox lane 1): the smallest x with C(x) >= u' * C(V-1), C the
 // prefix sum of the weights in token order.
 //
-// The CDF is evaluated in two levels so that only one chunk is ever scanned:
-//   level 1: per-chunk masses (residual: computed here, CH2 tokens per CTA
-//            unit; bonus: the row-stat partials of k_row_stats), prefix-summed
-//            in float64 in chunk order -> the chunk c* holding u' * C(V-1);
-//   level 2: the chunk c* is re-read, its weights recomputed with the same
-//            float32 expression as level 1, block-scanned in float64, and the
-//            first token whose running sum reaches the remaining mass is taken
-//            (zero-mass tokens are never taken; if rounding leaves the
-//            threshold beyond the chunk, its last token of positive mass is).
-// Residual chunk sums of one request are spread over CTAs; the CTA that
-// finishes the last one (atomic counter, threadfence pattern) runs level 2.
+// The CDF is evaluated in two levels so that only one 2048-token chunk is ever
+// scanned:
+//   level 1: per-chunk masses (residual: summed here, one warp per chunk;
+//            bonus: the row-stat partials of k_row_stats), prefix-summed in
+//            float64 in chunk order -> the chunk c* holding u' * C(V-1);
+//   level 2: the chunk c* is copied into shared memory, its weights recomputed
+//            with the same float32 expression as level 1, and scanned in token
+//            order (8-token groups, float32): the first token whose running sum
+//            reaches the remaining mass is taken.  Tokens of zero mass are
+//            never taken; if rounding leaves the threshold beyond the chunk,
+//            its last token of positive mass is.
+// Every unit of work belongs to one warp and warps never wait for each other.
+// k_sample: a residual unit is one chunk of (logits row, draft row) whose mass
+// is stored; the warp copies the chunk into shared memory with two 1-D bulk
+// copies (cp.async.bulk, mbarrier completion) while the previous unit is being
+// reduced (two stages per warp).  k_emit (the next kernel, once the memory
+// system is free of the streaming traffic): one warp per draw, residual or
+// bonus, runs both levels.
 #include <cfloat>
 #include <climits>
 
@@ -27,181 +34,80 @@ namespace sv {
 
 namespace {
 
-constexpr int NW = SAMPLE_THREADS / 32;
-
-struct Smem {
-    double red[NW];
-    int ired[NW];
-    double t_level2;
-    double mass;
-    int chunk;
-    int last;
+template <int DT>
+struct Stage {
+    static constexpr int ESZ = DT == SPEC_BF16 ? 2 : 4;
+    static constexpr int LB = TILE * ESZ;  // logits chunk
+    static constexpr int QB = TILE * 4;    // draft-probability chunk
+    static constexpr int BYTES = LB + QB;
 };
 
-__device__ __forceinline__ double block_sum(double v, Smem& sm) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v = warp_sum(v);
-    __syncthreads();
-    if (lane == 0) sm.red[warp] = v;
-    __syncthreads();
-    double s = 0.0;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) s += sm.red[w];  // same order in every thread
-    return s;
-}
-
-// Exclusive prefix (token order = thread order) of one double per thread.
-__device__ __forceinline__ double block_excl_scan(double v, Smem& sm) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    double incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    __syncthreads();
-    if (lane == 31) sm.red[warp] = incl;
-    __syncthreads();
-    double base = 0.0;
-    for (int w = 0; w < warp; ++w) base += sm.red[w];
-    return base + incl - v;
-}
-
-__device__ __forceinline__ int block_min_int(int v, Smem& sm) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v = warp_min_int(v);
-    __syncthreads();
-    if (lane == 0) sm.ired[warp] = v;
-    __syncthreads();
-    int r = INT_MAX;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) r = min(r, sm.ired[w]);
-    return r;
-}
-
-__device__ __forceinline__ int block_max_int(int v, Smem& sm) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v = warp_max_int(v);
-    __syncthreads();
-    if (lane == 0) sm.ired[warp] = v;
-    __syncthreads();
-    int r = INT_MIN;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) r = max(r, sm.ired[w]);
-    return r;
-}
-
-// max(0, p - q) with p = 2^((l - m) kappa) / Z; the same float32 operations
-// at both levels so that a token's weight is bit-identical in both.
-__device__ __forceinline__ float resid(float l, float q, float m, float kappa, float invZ) {
-    const float p = __fmul_rn(ex2_approx(__fmul_rn(__fsub_rn(l, m), kappa)), invZ);
+// max(0, p - q) with p = 2^((l - m) kappa) / Z, written against the row's
+// offset c = RN(m kappa) like every other weight of the row; the same float32
+// operations at both levels so that a token's weight is bit-identical in both.
+__device__ __forceinline__ float resid(float l, float q, float m, float c, float kappa,
+                                      float invZ) {
+    const float p = __fmul_rn(ex2_approx(weight_arg(l, m, c, kappa)), invZ);
     return fmaxf(__fsub_rn(p, q), 0.f);
 }
 
-// 8 consecutive logits starting at element e (e % 8 == 0), read-only path.
+// The 8 logits of group g of a staged chunk.
 template <int DT>
-__device__ __forceinline__ void load8(const void* logits, size_t e, float (&f)[8]) {
+__device__ __forceinline__ void smem_logits8(const uint8_t* st, int g, float (&f)[8]) {
     if constexpr (DT == SPEC_BF16) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-            reinterpret_cast<const uint16_t*>(logits) + e));
+        const uint4 v = reinterpret_cast<const uint4*>(st)[g];
         f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
         f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
         f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
         f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
     } else {
-        const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(logits) + e);
-        const float4 a = __ldg(p), c = __ldg(p + 1);
+        const float4 a = reinterpret_cast<const float4*>(st)[2 * g];
+        const float4 c = reinterpret_cast<const float4*>(st)[2 * g + 1];
         f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
         f[4] = c.x; f[5] = c.y; f[6] = c.z; f[7] = c.w;
     }
 }
-__device__ __forceinline__ void load8q(const float* q, size_t e, float (&f)[8]) {
-    const float4* p = reinterpret_cast<const float4*>(q + e);
-    const float4 a = __ldg(p), c = __ldg(p + 1);
+__device__ __forceinline__ void smem_q8(const uint8_t* stq, int g, float (&f)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(stq)[2 * g];
+    const float4 c = reinterpret_cast<const float4*>(stq)[2 * g + 1];
     f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
     f[4] = c.x; f[5] = c.y; f[6] = c.z; f[7] = c.w;
 }
 
-// Level 1 of the residual: mass of chunk c (CH2 tokens) of row rec.erow.
-template <int DT>
-__device__ double residual_chunk_sum(const Params& P, const ReqRec& rec, int c, Smem& sm) {
-    const size_t lrow = ((size_t)rec.b * P.K1 + rec.erow) * P.V;
-    const size_t qrow = ((size_t)rec.b * P.K + rec.erow) * P.V;
-    const float invZ = float(1.0 / rec.Z);
-    constexpr int G = CH2 / 8 / SAMPLE_THREADS;  // 8-token groups per thread
-    float gs[G];
-#pragma unroll
-    for (int k = 0; k < G; ++k) {
-        const int e0 = c * CH2 + (k * SAMPLE_THREADS + threadIdx.x) * 8;
-        gs[k] = 0.f;
-        if (e0 < P.V) {
-            float l[8], q[8], r[8];
-            load8<DT>(P.logits, lrow + e0, l);
-            load8q(P.probs, qrow + e0, q);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) r[e] = resid(l[e], q[e], rec.m, rec.kappa, invZ);
-#pragma unroll
-            for (int h = 4; h; h >>= 1)
-#pragma unroll
-                for (int e = 0; e < h; ++e) r[e] = __fadd_rn(r[e], r[e + h]);
-            gs[k] = r[0];
-        }
-    }
-#pragma unroll
-    for (int h = G / 2; h; h >>= 1)
-#pragma unroll
-        for (int k = 0; k < h; ++k) gs[k] = __fadd_rn(gs[k], gs[k + h]);
-    return block_sum(double(gs[0]), sm);
-}
+// The per-warp double-buffered staging area.
+struct WarpStages {
+    uint8_t* base;      // stage s starts at base + s * stage_bytes
+    uint64_t* bars;     // bars[s]
+    int stage_bytes;
+    uint32_t phase;     // bit s: phase of stage s's barrier
+    uint32_t inflight;  // bit s: a copy into stage s has not been waited for
+    bool broken;        // a bounded wait gave up
 
-// Level 1 over `nc` chunk masses mass(c) (c in order): total S = last prefix,
-// then the first chunk whose prefix reaches u * S.  Run by warp 0; results in sm.
-template <typename MassFn>
-__device__ void pick_chunk(int nc, float u, MassFn mass, Smem& sm) {
-    const int lane = threadIdx.x & 31;
-    if (threadIdx.x >= 32) return;
-    double carry = 0.0;
-    for (int c0 = 0; c0 < nc; c0 += 32) {
-        double v = c0 + lane < nc ? mass(c0 + lane) : 0.0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += y;
-        }
-        carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-    const double S = carry;
-    const double t = double(u) * S;
-    int chosen = -1;
-    double before = 0.0;
-    carry = 0.0;
-    for (int c0 = 0; c0 < nc && chosen < 0; c0 += 32) {
-        const double m = c0 + lane < nc ? mass(c0 + lane) : 0.0;
-        double v = m;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += y;
-        }
-        const double incl = carry + v;
-        const unsigned hit = __ballot_sync(0xffffffffu, c0 + lane < nc && incl >= t && m > 0.0);
-        const double prev = __shfl_up_sync(0xffffffffu, incl, 1);
-        if (hit) {
-            const int l = __ffs(hit) - 1;
-            chosen = c0 + l;
-            before = __shfl_sync(0xffffffffu, lane == 0 ? carry : prev, l);
-        }
-        carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-    if (lane == 0) {
-        sm.mass = S;
-        sm.chunk = chosen;
-        sm.t_level2 = t - before;
-    }
-}
+    __device__ __forceinline__ uint8_t* buf(int s) const { return base + s * stage_bytes; }
 
-template <int DT>
-__device__ void write_emit(const Params& P, const ReqRec& rec, int x, int mode, double mass) {
+    // lane 0: copy `bl` bytes of logits (and `bq` of q) into stage s
+    __device__ __forceinline__ void issue(int s, const void* l, uint32_t bl, const void* q,
+                                          uint32_t bq, int lb_offset) {
+        if ((threadIdx.x & 31) == 0) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bars + s, bl + bq);
+            bulk_g2s(buf(s), l, bl, bars + s);
+            if (bq) bulk_g2s(buf(s) + lb_offset, q, bq, bars + s);
+        }
+        inflight |= 1u << s;
+    }
+    // whole warp: wait for stage s (bounded); false if the wait gave up
+    __device__ __forceinline__ bool wait(int s) {
+        const bool ok = mbar_wait_bounded(bars + s, (phase >> s) & 1u);
+        phase ^= 1u << s;
+        inflight &= ~(1u << s);
+        return __all_sync(0xffffffffu, ok);
+    }
+};
+
+__device__ __forceinline__ void write_emit(const Params& P, const ReqRec& rec, int x, int mode,
+                                           double mass) {
+    if ((threadIdx.x & 31) != 0) return;
     P.out_ids[(size_t)rec.b * P.K1 + rec.erow] = x;
     if (P.dbg_req) {
         float* d = P.dbg_req + (size_t)rec.b * 4;
@@ -212,156 +118,374 @@ __device__ void write_emit(const Params& P, const ReqRec& rec, int x, int mode, 
     }
 }
 
-// Draw from p of row rec.erow using the row-stat partials (bonus token, or the
-// residual when it has no mass).
-template <int DT>
-__device__ void emit_from_p(const Params& P, const ReqRec& rec, int mode, Smem& sm) {
-    const Partial* part = P.part + ((size_t)rec.b * P.K1 + rec.erow) * P.C;
-    const float m = rec.m, kappa = rec.kappa;
-    auto wmass = [&](int c) -> double {
-        const Partial q = part[c];
-        if (q.m == -INFINITY || q.z == 0.0) return 0.0;
-        return q.z * exp2(double(__fmul_rn(__fsub_rn(q.m, m), kappa)));
-    };
-    pick_chunk(P.C, rec.u2, wmass, sm);
-    __syncthreads();
-    const int c = sm.chunk;
-    const double S = sm.mass;
-    if (c < 0) {  // no mass at all (cannot happen for a row with a finite logit)
-        if (threadIdx.x == 0) write_emit<DT>(P, rec, 0, mode, S);
-        __syncthreads();
-        return;
+struct Pick {
+    int chunk;      // chosen chunk, -1 if the total mass is not positive
+    double before;  // mass of the chunks before it
+    double total;   // total mass S (the last prefix)
+};
+
+__device__ __forceinline__ double warp_incl_scan(double x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
     }
-    const Partial pc = part[c];
-    const double f_c = exp2(double(__fmul_rn(__fsub_rn(pc.m, m), kappa)));
-    const double t = sm.t_level2 / f_c;  // remaining mass in the chunk's own scale
-    // level 2: TILE tokens, TILE / SAMPLE_THREADS consecutive tokens per thread
-    constexpr int PT = TILE / SAMPLE_THREADS;
-    const size_t lrow = ((size_t)rec.b * P.K1 + rec.erow) * P.V;
-    const int e0 = c * TILE + threadIdx.x * PT;
-    float w[PT];
-    double ts = 0.0;
-#pragma unroll
-    for (int k = 0; k < PT; k += 8) {
-        float l[8];
-        if (e0 + k < P.V) {
-            load8<DT>(P.logits, lrow + e0 + k, l);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) l[e] = -INFINITY;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            w[k + e] = ex2_approx(__fmul_rn(__fsub_rn(l[e], pc.m), kappa));
-            ts += double(w[k + e]);
-        }
-    }
-    double acc = block_excl_scan(ts, sm);
-    int cand = INT_MAX, lastpos = INT_MIN;
-#pragma unroll
-    for (int k = 0; k < PT; ++k) {
-        acc += double(w[k]);
-        if (w[k] > 0.f) {
-            lastpos = e0 + k;
-            if (cand == INT_MAX && acc >= t) cand = e0 + k;
-        }
-    }
-    int x = block_min_int(cand, sm);
-    if (x == INT_MAX) x = block_max_int(lastpos, sm);
-    if (threadIdx.x == 0) write_emit<DT>(P, rec, x == INT_MIN ? c * TILE : x, mode, S);
-    __syncthreads();
+    return x;
 }
 
-// Level 2 of the residual for queued request i (run by the CTA that finished
-// its last chunk sum).
-template <int DT>
-__device__ void emit_residual(const Params& P, const ReqRec& rec, int i, Smem& sm) {
-    const double* rs = P.rsum + (size_t)i * P.C2;
-    pick_chunk(P.C2, rec.u2, [&](int c) -> double { return __ldcg(rs + c); }, sm);
-    __syncthreads();
-    const int c = sm.chunk;
-    const double S = sm.mass;
-    if (c < 0 || !(S > 0.0)) {  // residual without mass: draw from p instead
-        __syncthreads();
-        emit_from_p<DT>(P, rec, MODE_FALLBACK, sm);
-        return;
-    }
-    const double t = sm.t_level2;
-    const float invZ = float(1.0 / rec.Z);
-    constexpr int PT = CH2 / SAMPLE_THREADS;  // consecutive tokens per thread
-    const size_t lrow = ((size_t)rec.b * P.K1 + rec.erow) * P.V;
-    const size_t qrow = ((size_t)rec.b * P.K + rec.erow) * P.V;
-    const int e0 = c * CH2 + threadIdx.x * PT;
-    float r[PT];
-    double ts = 0.0;
+// Level 1 over nc chunk masses mass(c) in chunk order, by one warp: S = the
+// last prefix; the chosen chunk is the first whose prefix reaches u * S.
+// Up to 128 chunks are loaded at once (one round trip); beyond, block by block.
+template <typename MassFn>
+__device__ __forceinline__ Pick pick_chunk(int nc, float u, MassFn mass) {
+    const int lane = threadIdx.x & 31;
+    constexpr int NB = 4;
+    Pick pk;
+    pk.chunk = -1;
+    pk.before = 0.0;
+    if (nc <= NB * 32) {
+        double v[NB], incl[NB];
 #pragma unroll
-    for (int k = 0; k < PT; k += 8) {
-        if (e0 + k < P.V) {
-            float l[8], q[8];
-            load8<DT>(P.logits, lrow + e0 + k, l);
-            load8q(P.probs, qrow + e0 + k, q);
+        for (int i = 0; i < NB; ++i) v[i] = i * 32 + lane < nc ? mass(i * 32 + lane) : 0.0;
+        double carry = 0.0;
+#pragma unroll 1
+        for (int i = 0; i < NB; ++i) {
+            incl[i] = carry + warp_incl_scan(v[i]);
+            carry = __shfl_sync(0xffffffffu, incl[i], 31);
+        }
+        pk.total = carry;
+        if (!(carry > 0.0)) return pk;
+        const double t = double(u) * carry;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const double prev = __shfl_up_sync(0xffffffffu, incl[i], 1);
+            const double first = i == 0 ? 0.0 : __shfl_sync(0xffffffffu, incl[i == 0 ? 0 : i - 1], 31);
+            const unsigned hit = __ballot_sync(0xffffffffu, incl[i] >= t && v[i] > 0.0);
+            if (hit && pk.chunk < 0) {
+                const int l = __ffs(hit) - 1;
+                pk.chunk = i * 32 + l;
+                pk.before = __shfl_sync(0xffffffffu, lane == 0 ? first : prev, l);
+            }
+        }
+        return pk;
+    }
+    double carry = 0.0;
+    for (int c0 = 0; c0 < nc; c0 += 32)
+        carry = carry + __shfl_sync(0xffffffffu,
+                                    warp_incl_scan(c0 + lane < nc ? mass(c0 + lane) : 0.0), 31);
+    pk.total = carry;
+    if (!(carry > 0.0)) return pk;
+    const double t = double(u) * carry;
+    carry = 0.0;
+    for (int c0 = 0; c0 < nc; c0 += 32) {
+        const double m = c0 + lane < nc ? mass(c0 + lane) : 0.0;
+        const double incl = carry + warp_incl_scan(m);
+        const double prev = __shfl_up_sync(0xffffffffu, incl, 1);
+        const unsigned hit = __ballot_sync(0xffffffffu, c0 + lane < nc && incl >= t && m > 0.0);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            pk.chunk = c0 + l;
+            pk.before = __shfl_sync(0xffffffffu, lane == 0 ? carry : prev, l);
+            break;
+        }
+        carry = __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return pk;
+}
+
+// Level 2 over a staged chunk of nel tokens starting at token c0: weight8(g, w)
+// gives the weights of 8-token group g (same expression as level 1).  Groups
+// are visited in token order g = 32 k + lane; returns the first token whose
+// running sum reaches t, or the chunk's last token of positive mass.
+template <typename WeightFn>
+__device__ __noinline__ int level2(int c0, int nel, float t, WeightFn weight8) {
+    const int lane = threadIdx.x & 31;
+    constexpr int G = TILE / 8 / 32;
+    float gsum[G];
+    int glast[G];  // last positive token of the group (-1: none)
+#pragma unroll 1
+    for (int k = 0; k < G; ++k) {
+        const int g = k * 32 + lane;
+        gsum[k] = 0.f;
+        glast[k] = -1;
+        if (g * 8 < nel) {
+            float w[8];
+            weight8(g, w);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                r[k + e] = resid(l[e], q[e], rec.m, rec.kappa, invZ);
-                ts += double(r[k + e]);
+                gsum[k] = __fadd_rn(gsum[k], w[e]);
+                if (w[e] > 0.f) glast[k] = g * 8 + e;
             }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) r[k + e] = 0.f;
         }
     }
-    double acc = block_excl_scan(ts, sm);
-    int cand = INT_MAX, lastpos = INT_MIN;
+    float carry = 0.f;
+    int found = -1;
+    float before = 0.f;
+#pragma unroll 1
+    for (int k = 0; k < G; ++k) {
+        float incl = gsum[k];
 #pragma unroll
-    for (int k = 0; k < PT; ++k) {
-        acc += double(r[k]);
-        if (r[k] > 0.f) {
-            lastpos = e0 + k;
-            if (cand == INT_MAX && acc >= t) cand = e0 + k;
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl = __fadd_rn(incl, y);
+        }
+        incl = __fadd_rn(carry, incl);
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= t && gsum[k] > 0.f);
+        if (hit && found < 0) {
+            const int l = __ffs(hit) - 1;
+            found = k * 32 + l;
+            before = __shfl_sync(0xffffffffu, __fsub_rn(incl, gsum[k]), l);
+        }
+        carry = __shfl_sync(0xffffffffu, incl, 31);
+    }
+    int x = -1;
+    if (found >= 0) {
+        if (lane == (found & 31)) {  // the owning lane walks its group
+            float w[8];
+            weight8(found, w);
+            float run = before;
+            int lastpos = -1;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                run = __fadd_rn(run, w[e]);
+                if (w[e] > 0.f) {
+                    lastpos = found * 8 + e;
+                    if (x < 0 && run >= t) x = found * 8 + e;
+                }
+            }
+            if (x < 0) x = lastpos;
+        }
+        x = __shfl_sync(0xffffffffu, x, found & 31);
+    } else {
+        int last = -1;
+#pragma unroll
+        for (int k = 0; k < G; ++k) last = max(last, glast[k]);
+        x = warp_max_int(last);
+    }
+    return c0 + (x < 0 ? 0 : x);
+}
+
+// Draw from p of row rec.erow using the row-stat partials (bonus token, or the
+// residual when it has no mass).  Level 2 stages the chunk in stage s.
+template <int DT>
+__device__ void emit_from_p(const Params& P, const ReqRec& rec, int mode, WarpStages& ws, int s) {
+    const Partial* part = P.part + ((size_t)rec.b * P.K1 + rec.erow) * P.C;
+    const float m = rec.m, kappa = rec.kappa;
+    const Pick pk = pick_chunk(P.C, rec.u2, [&](int c) -> double {
+        const Partial q = part[c];
+        if (q.m == -INFINITY || q.z == 0.0) return 0.0;
+        return q.z * double(exp2f(rebase_arg(q.m, m, kappa)));
+    });
+    if (pk.chunk < 0) {  // no mass at all (cannot happen for a row with a finite logit)
+        write_emit(P, rec, 0, mode, pk.total);
+        return;
+    }
+    const Partial pc = part[pk.chunk];
+    const double f_c = double(exp2f(rebase_arg(pc.m, m, kappa)));
+    const float t = float((double(rec.u2) * pk.total - pk.before) / f_c);  // chunk-local mass
+    const float cc = offset_of(pc.m, kappa);
+    const int c0 = pk.chunk * TILE, nel = min(TILE, P.V - c0);
+    const char* src = reinterpret_cast<const char*>(P.logits) +
+                      (((size_t)rec.b * P.K1 + rec.erow) * P.V + c0) * Stage<DT>::ESZ;
+    ws.issue(s, src, uint32_t(nel) * Stage<DT>::ESZ, nullptr, 0, Stage<DT>::LB);
+    if (!ws.wait(s)) {
+        ws.broken = true;
+        return;
+    }
+    const uint8_t* st = ws.buf(s);
+    const int x = level2(c0, nel, t, [&](int g, float (&w)[8]) {
+        float l[8];
+        smem_logits8<DT>(st, g, l);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = ex2_approx(weight_arg(l[k], pc.m, cc, kappa));
+    });
+    __syncwarp();
+    write_emit(P, rec, x, mode, pk.total);
+}
+
+// Residual mass of a staged chunk of nel tokens (coalesced 8-token groups,
+// pairwise float32 sums, warp shuffle sum).
+template <int DT>
+__device__ __forceinline__ float staged_residual_sum(const uint8_t* st, int nel, const ReqRec& rec) {
+    const int lane = threadIdx.x & 31;
+    const float invZ = float(1.0 / rec.Z);
+    const float cm = offset_of(rec.m, rec.kappa);
+    constexpr int G = TILE / 8 / 32;
+    float gs[G];
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+        const int g = k * 32 + lane;
+        gs[k] = 0.f;
+        if (g * 8 < nel) {
+            float l[8], q[8];
+            smem_logits8<DT>(st, g, l);
+            smem_q8(st + Stage<DT>::LB, g, q);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) l[e] = resid(l[e], q[e], rec.m, cm, rec.kappa, invZ);
+#pragma unroll
+            for (int h = 4; h; h >>= 1)
+#pragma unroll
+                for (int e = 0; e < h; ++e) l[e] = __fadd_rn(l[e], l[e + h]);
+            gs[k] = l[0];
         }
     }
-    int x = block_min_int(cand, sm);
-    if (x == INT_MAX) x = block_max_int(lastpos, sm);
-    if (threadIdx.x == 0) write_emit<DT>(P, rec, x == INT_MIN ? c * CH2 : x, MODE_RESIDUAL, S);
-    __syncthreads();
+#pragma unroll
+    for (int h = G / 2; h; h >>= 1)
+#pragma unroll
+        for (int k = 0; k < h; ++k) gs[k] = __fadd_rn(gs[k], gs[k + h]);
+    return warp_sum_f(gs[0]);
+}
+
+// Level 1 and 2 of the residual of queued request i, by the warp that
+// completed its last chunk sum.  Level 2 stages the chunk in stage s.
+template <int DT>
+__device__ void emit_residual(const Params& P, const ReqRec& rec, int i, WarpStages& ws, int s) {
+    const float* rs = P.rsum + (size_t)i * P.C;
+    const Pick pk = pick_chunk(P.C, rec.u2, [&](int c) -> double { return double(__ldcg(rs + c)); });
+    if (pk.chunk < 0) {  // residual without mass: draw from p instead
+        emit_from_p<DT>(P, rec, MODE_FALLBACK, ws, s);
+        return;
+    }
+    const float t = float(double(rec.u2) * pk.total - pk.before);
+    const float invZ = float(1.0 / rec.Z);
+    const float cm = offset_of(rec.m, rec.kappa);
+    const int c0 = pk.chunk * TILE, nel = min(TILE, P.V - c0);
+    const char* l = reinterpret_cast<const char*>(P.logits) +
+                    (((size_t)rec.b * P.K1 + rec.erow) * P.V + c0) * Stage<DT>::ESZ;
+    const float* q = P.probs + ((size_t)rec.b * P.K + rec.erow) * P.V + c0;
+    ws.issue(s, l, uint32_t(nel) * Stage<DT>::ESZ, q, uint32_t(nel) * 4u, Stage<DT>::LB);
+    if (!ws.wait(s)) {
+        ws.broken = true;
+        return;
+    }
+    const uint8_t* st = ws.buf(s);
+    const int x = level2(c0, nel, t, [&](int g, float (&w)[8]) {
+        float lv[8], qv[8];
+        smem_logits8<DT>(st, g, lv);
+        smem_q8(st + Stage<DT>::LB, g, qv);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = resid(lv[k], qv[k], rec.m, cm, rec.kappa, invZ);
+    });
+    __syncwarp();
+    write_emit(P, rec, x, MODE_RESIDUAL, pk.total);
 }
 
 }  // namespace
 
+// Per-warp staging setup.
 template <int DT>
-__device__ __forceinline__ void sample_body(const Params& P) {
-    __shared__ Smem sm;
-    griddep_launch_dependents();
-    griddep_wait();  // decisions and queues of k_accept
-    const int n_res = P.hdr[HDR_NRES], n_bonus = P.hdr[HDR_NBONUS];
-    const long long res_units = (long long)n_res * P.C2;
-    const long long units = res_units + n_bonus;
-    for (long long unit = blockIdx.x; unit < units; unit += gridDim.x) {
-        if (unit < res_units) {
-            const int i = int(unit / P.C2), c = int(unit - (long long)i * P.C2);
-            const ReqRec rec = P.reqs[P.res_list[i]];
-            const double s = residual_chunk_sum<DT>(P, rec, c, sm);
-            if (threadIdx.x == 0) {
-                P.rsum[(size_t)i * P.C2 + c] = s;
-                __threadfence();
-                sm.last = (atomicAdd(&P.res_cnt[i], 1) == P.C2 - 1);
-            }
-            __syncthreads();
-            const bool last = sm.last;
-            __syncthreads();
-            if (last) {
-                __threadfence();
-                emit_residual<DT>(P, rec, i, sm);
-            }
-        } else {
-            const ReqRec rec = P.reqs[P.bonus_list[unit - res_units]];
-            emit_from_p<DT>(P, rec, MODE_BONUS, sm);
-        }
-        __syncthreads();
+__device__ __forceinline__ WarpStages make_stages(uint8_t* smem, uint64_t* bars, int nstages) {
+    using ST = Stage<DT>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    WarpStages ws;
+    ws.base = smem + size_t(warp) * nstages * ST::BYTES;
+    ws.bars = bars + warp * 2;
+    ws.stage_bytes = ST::BYTES;
+    ws.phase = 0;
+    ws.inflight = 0;
+    ws.broken = false;
+    if (lane == 0) {
+        for (int k = 0; k < nstages; ++k) mbar_init(ws.bars + k, 1);
+        fence_mbarrier_init();
+    }
+    __syncwarp();
+    return ws;
+}
+
+__device__ __forceinline__ void finish_stages(const Params& P, WarpStages& ws) {
+    if (ws.broken) {
+        if ((threadIdx.x & 31) == 0) atomicOr(P.status, int(SPEC_BADBIT_TIMEOUT));
+        // let copies still in flight land before the CTA's shared memory is released
+        for (int k = 0; k < 2; ++k)
+            if (ws.inflight & (1u << k))
+                mbar_wait_bounded(ws.bars + k, (ws.phase >> k) & 1u, 100000000ull);
     }
 }
 
-__global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_f32(Params P) { sample_body<SPEC_F32>(P); }
-__global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_bf16(Params P) { sample_body<SPEC_BF16>(P); }
+// k_sample: the residual chunk masses of every queued request, one warp per
+// 2048-token chunk.  Each warp takes an equal contiguous range of the units
+// (queue entry i, chunk c) in order and keeps two staging buffers: the next
+// chunk's bulk copies are in flight while the current one is reduced.  A pure
+// streaming pass: the draws themselves are made by k_emit.
+template <int DT>
+__device__ __forceinline__ void sample_body(const Params& P) {
+    using ST = Stage<DT>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[SAMPLE_WARPS * 2];
+    WarpStages ws = make_stages<DT>(smem, bars, 2);
+    griddep_launch_dependents();
+    griddep_wait();  // decisions and queues of the acceptance step
+    const int lane = threadIdx.x & 31;
+    const long long W = (long long)gridDim.x * SAMPLE_WARPS;
+    const long long wid = (long long)blockIdx.x * SAMPLE_WARPS + (threadIdx.x >> 5);
+    const long long VT = (long long)P.hdr[HDR_NRES] * P.C;
+    const long long r0 = VT * wid / W, r1 = VT * (wid + 1) / W;
+    auto issue_res = [&](long long v, const ReqRec& r, int s) {
+        const int c = int(v % P.C);
+        const int c0 = c * TILE, nel = min(TILE, P.V - c0);
+        const char* l = reinterpret_cast<const char*>(P.logits) +
+                        (((size_t)r.b * P.K1 + r.erow) * P.V + c0) * ST::ESZ;
+        const float* q = P.probs + ((size_t)r.b * P.K + r.erow) * P.V + c0;
+        ws.issue(s, l, uint32_t(nel) * ST::ESZ, q, uint32_t(nel) * 4u, ST::LB);
+    };
+    if (r0 < r1) {
+        int s = 0;
+        ReqRec cur = P.res_rec[r0 / P.C];
+        issue_res(r0, cur, s);
+        for (long long v = r0; v < r1; ++v) {
+            const long long i = v / P.C;
+            const int c = int(v - i * P.C);
+            const long long next = v + 1;
+            ReqRec nxt = cur;
+            if (next < r1) {  // stage the next chunk while this one is reduced
+                if (next / P.C != i) nxt = P.res_rec[next / P.C];
+                issue_res(next, nxt, s ^ 1);
+            }
+            if (!ws.wait(s)) {
+                ws.broken = true;
+                break;
+            }
+            const float sum = staged_residual_sum<DT>(ws.buf(s), min(TILE, P.V - c * TILE), cur);
+            __syncwarp();  // stage s has been read
+            if (lane == 0) P.rsum[(size_t)i * P.C + c] = sum;
+            cur = nxt;
+            s ^= 1;
+        }
+    }
+    finish_stages(P, ws);
+}
+
+// k_emit: one warp per draw once every residual mass exists: the residual
+// draws of the rejecting requests, then the bonus draws of the requests whose
+// drafts were all accepted.
+template <int DT>
+__device__ __forceinline__ void emit_body(const Params& P) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[SAMPLE_WARPS * 2];
+    WarpStages ws = make_stages<DT>(smem, bars, 1);
+    griddep_launch_dependents();
+    griddep_wait();  // chunk masses of k_sample
+    const long long W = (long long)gridDim.x * SAMPLE_WARPS;
+    const int n_res = P.hdr[HDR_NRES], n_bonus = P.hdr[HDR_NBONUS];
+    for (long long k = (long long)blockIdx.x * SAMPLE_WARPS + (threadIdx.x >> 5);
+         k < n_res + n_bonus && !ws.broken; k += W) {
+        if (k < n_res)
+            emit_residual<DT>(P, P.res_rec[k], int(k), ws, 0);
+        else
+            emit_from_p<DT>(P, P.bonus_rec[k - n_res], MODE_BONUS, ws, 0);
+    }
+    finish_stages(P, ws);
+}
+
+__global__ void __launch_bounds__(SAMPLE_WARPS * 32) k_sample_f32(Params P) {
+    sample_body<SPEC_F32>(P);
+}
+__global__ void __launch_bounds__(SAMPLE_WARPS * 32) k_sample_bf16(Params P) {
+    sample_body<SPEC_BF16>(P);
+}
+__global__ void __launch_bounds__(SAMPLE_WARPS * 32) k_emit_f32(Params P) { emit_body<SPEC_F32>(P); }
+__global__ void __launch_bounds__(SAMPLE_WARPS * 32) k_emit_bf16(Params P) { emit_body<SPEC_BF16>(P); }
+
 
 }  // namespace sv
