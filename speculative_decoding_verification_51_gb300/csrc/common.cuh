@@ -57,7 +57,7 @@ struct __align__(16) Partial {
     double z;    // sampling rows: sum exp2((l - m) * kappa) over the chunk
 };
 
-// A queued sampling draw, written by k_accept.
+// A queued sampling draw, written by the acceptance step.
 struct __align__(16) ReqRec {
     int mode;     // MODE_*
     int erow;     // row the emitted token is drawn from
@@ -284,6 +284,19 @@ __device__ __forceinline__ double warp_sum(double v) {
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
+// Single-instruction warp reductions (sm_100 family): max of f32 (NaN inputs
+// ignored) and min of s32 over all 32 lanes.
+__device__ __forceinline__ float redux_max_f32(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ int redux_min_s32(int v) {
+    int r;
+    asm volatile("redux.sync.min.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
+}
+
 __device__ __forceinline__ int warp_min_int(int v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -14,10 +14,13 @@
 // copy (cp.async.bulk, completion on a per-stage mbarrier) for the tile
 // STATS_STAGES ahead while the warp reduces the current tile out of shared
 // memory (16-byte loads, 64 tokens per lane):
-//   sampling rows: chunk max by a packed bf16x2 max tree and shuffles, then
-//     the sum of 2^(l * kappa - c) with c = RN(max * kappa) (one FFMA and one
-//     ex2 per token, pairwise float32 sums, shuffles);
-//   greedy rows: chunk max, then the lowest index attaining it.
+//   sampling rows: each lane takes its maximum by a packed bf16x2 max tree and
+//     sums 2^(l * kappa - c) against its own offset c = RN(max * kappa) (one
+//     FFMA and one ex2 per token, pairwise float32 sums); the chunk maximum is
+//     one redux.sync, each lane's sum is rebased onto it with one ex2, and the
+//     lanes are summed by shuffles.  The stored sum is relative to the chunk's
+//     offset RN(chunk max * kappa), as every consumer expects;
+//   greedy rows: chunk max (redux), then the lowest index attaining it.
 // While the tile holding the draft token x_j of a row is in shared memory its
 // logit is copied out, and q_j(x_j) is fetched, for the acceptance test.
 // No block-wide barrier and no float64 arithmetic (the FP64 pipe of this part
@@ -110,7 +113,7 @@ __device__ __forceinline__ RowCtx row_ctx(const Params& P, long long r) {
     int x = -1;
     if (!rc.greedy && j < rc.n) {
         x = P.ids[(size_t)b * P.K + j];
-        if (x < 0 || x >= P.V) x = -1;  // reported by k_accept
+        if (x < 0 || x >= P.V) x = -1;  // reported by the acceptance step
     }
     rc.xj = x;
     rc.xchunk = x >= 0 ? x / TILE : -1;
@@ -240,12 +243,12 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
         }
 
         const int tok0 = cc * TILE;
-        const float m = warp_max(lane_max<DT>(d));
+        const float lmax = lane_max<DT>(d);
         Partial out;
-        out.m = m;
         if (rc.greedy) {
-            // lowest index attaining m: visiting tokens from high to low index
-            // leaves the lowest hit
+            // lowest index attaining the tile max: visiting tokens from high to
+            // low index leaves the lowest hit
+            const float m = redux_max_f32(lmax);
             int bidx = INT_MAX;
 #pragma unroll
             for (int k = VPL - 1; k >= 0; --k) {
@@ -257,34 +260,37 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
                         if (f[e] == m) bidx = tok0 + (k * 32 + lane) * EPV + e;
                 }
             }
-            out.amax = warp_min_int(bidx);
+            out.m = m;
+            out.amax = redux_min_s32(bidx);
             out.z = 0.0;
         } else {
-            float z = 0.f;
-            if (m != -INFINITY) {
-                const float c = offset_of(m, rc.kappa);
+            // each lane sums against its own maximum, so the ex2 loop does not
+            // wait for the warp-wide maximum; one rescale per lane follows
+            float zl = 0.f;
+            if (lmax != -INFINITY) {
+                const float cl = offset_of(lmax, rc.kappa);
                 float zs[VPL];
-                if (isfinite(c)) {  // one FFMA + ex2 per token
+                if (isfinite(cl)) {  // one FFMA + ex2 per token
 #pragma unroll
                     for (int k = 0; k < VPL; ++k) {
                         float f[EPV];
                         unpack<DT>(d[k], f);
 #pragma unroll
-                        for (int e = 0; e < EPV; ++e) f[e] = ex2_approx(fmaf(f[e], rc.kappa, -c));
+                        for (int e = 0; e < EPV; ++e) f[e] = ex2_approx(fmaf(f[e], rc.kappa, -cl));
 #pragma unroll
                         for (int h = EPV / 2; h; h >>= 1)
 #pragma unroll
                             for (int e = 0; e < h; ++e) f[e] = __fadd_rn(f[e], f[e + h]);
                         zs[k] = f[0];
                     }
-                } else {  // offset overflows (absurdly small T): (l - m) * kappa
+                } else {  // offset overflows (absurdly small T): (l - max) * kappa
 #pragma unroll
                     for (int k = 0; k < VPL; ++k) {
                         float f[EPV];
                         unpack<DT>(d[k], f);
 #pragma unroll
                         for (int e = 0; e < EPV; ++e)
-                            f[e] = ex2_approx(__fmul_rn(__fsub_rn(f[e], m), rc.kappa));
+                            f[e] = ex2_approx(__fmul_rn(__fsub_rn(f[e], lmax), rc.kappa));
 #pragma unroll
                         for (int h = EPV / 2; h; h >>= 1)
 #pragma unroll
@@ -296,10 +302,13 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
                 for (int h = VPL / 2; h; h >>= 1)
 #pragma unroll
                     for (int k = 0; k < h; ++k) zs[k] = __fadd_rn(zs[k], zs[k + h]);
-                z = warp_sum_f(zs[0]);
+                zl = zs[0];
             }
+            const float m = redux_max_f32(lmax);
+            if (zl != 0.f) zl = __fmul_rn(zl, ex2_approx(rebase_arg(lmax, m, rc.kappa)));
+            out.m = m;
             out.amax = -1;
-            out.z = double(z);
+            out.z = double(warp_sum_f(zl));
         }
         if (lane == 0) {
             P.part[(size_t)rc.slot * P.C + cc] = out;
