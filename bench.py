@@ -289,11 +289,12 @@ def main():
     _build.build()
     binding.lib()
 
+    from speculative_decoding_verification_51_gb300 import sharding
     w = W.make_workload(args.config, device=dev)
     if args.batch:
         w = w.leading(args.batch)
     B, K, V = w.B, w.K, w.V
-    offset = rank * B  # each rank holds its own requests of the global batch
+    offset = sharding.weak_offset(rank, B)  # each rank holds its own requests
     pos = W.positions(w.num_draft)
     ws = binding.new_workspace(B, K, V, dev)
     out_ids = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
@@ -341,10 +342,7 @@ def main():
         torch.distributed.barrier()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = sharding.max_over_ranks(ms, device=dev)
     clocks = clk.summary()
 
     # ---- per-kernel durations (same workload, marks between the kernels)
