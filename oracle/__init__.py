@@ -36,7 +36,8 @@ ROW_W = 4  # per-row diagnostics: p(x_j), q(x_j), u_j, accepted (-1 untested)
 R_PX, R_QX, R_U, R_ACCEPT = 0, 1, 2, 3
 REQ_W = 9  # per-request: mode, n_acc, emit row, u', mass, lo, hi, probe lo, probe hi
 Q_MODE, Q_NACC, Q_EROW, Q_UEMIT, Q_MASS, Q_LO, Q_HI, Q_PLO, Q_PHI = range(9)
-MODE_BAD, MODE_GREEDY, MODE_RESIDUAL, MODE_BONUS, MODE_FALLBACK = -1, 0, 1, 2, 3
+MODE_BAD, MODE_GREEDY, MODE_RESIDUAL, MODE_BONUS, MODE_FALLBACK, MODE_TYPICAL = -1, 0, 1, 2, 3, 4
+RULE_LOSSLESS, RULE_TYPICAL = 0, 1
 
 CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off", "-fno-fast-math"]
 
@@ -63,6 +64,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_spec_verify.restype = i32
     lib.oracle_spec_verify.argtypes = [vp, i32, vp, vp, vp, vp, u64, i32, i32, i32,
                                        vp, vp, vp, vp, vp, vp, vp, i32]
+    lib.oracle_spec_verify_rule.restype = i32
+    lib.oracle_spec_verify_rule.argtypes = [vp, i32, vp, vp, vp, vp, u64, i32, i32, i32,
+                                            vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                            ctypes.c_double]
     lib.oracle_philox_blocks.restype = None
     lib.oracle_philox_blocks.argtypes = [vp, vp, i64, vp]
     lib.oracle_row_uniforms.restype = None
@@ -93,7 +98,8 @@ def spec_verify(target_logits: np.ndarray, draft_probs: np.ndarray | None,
                 draft_ids: np.ndarray, num_draft: np.ndarray, temperature: np.ndarray,
                 seed: int, *, logits_dtype: str | None = None,
                 req_index: np.ndarray | None = None, uniforms: np.ndarray | None = None,
-                probe: np.ndarray | None = None, n_threads: int = 0, lib=None) -> dict:
+                probe: np.ndarray | None = None, n_threads: int = 0, lib=None,
+                typical_threshold: float | None = None) -> dict:
     """Run the oracle.
 
     target_logits: [B, K+1, V] float32, or uint16 bf16 bit patterns.
@@ -102,6 +108,8 @@ def spec_verify(target_logits: np.ndarray, draft_probs: np.ndarray | None,
     uniforms: None (Philox(seed, b, j)) or [B, K+1, 2] float64 used as given.
     req_index: global request index per local request (Philox counter).
     probe: [B] int32 token ids whose emission-CDF interval is reported.
+    typical_threshold: None for the lossless rule, else the hard threshold of
+    the typical-acceptance rule.
     """
     lib = lib or load()
     tl = np.ascontiguousarray(target_logits)
@@ -128,10 +136,17 @@ def spec_verify(target_logits: np.ndarray, draft_probs: np.ndarray | None,
     out_nacc = np.empty((B,), dtype=np.int32)
     row_diag = np.empty((B, K1, ROW_W), dtype=np.float64)
     req_diag = np.empty((B, REQ_W), dtype=np.float64)
-    n_bad = lib.oracle_spec_verify(_ptr(tl), dt, _ptr(dp), _ptr(di), _ptr(nd), _ptr(tp),
-                                   ctypes.c_uint64(seed & (2**64 - 1)), B, K, V, _ptr(ri),
-                                   _ptr(un), _ptr(pr), _ptr(out_ids), _ptr(out_nacc),
-                                   _ptr(row_diag), _ptr(req_diag), int(n_threads))
+    if typical_threshold is None:
+        n_bad = lib.oracle_spec_verify(_ptr(tl), dt, _ptr(dp), _ptr(di), _ptr(nd), _ptr(tp),
+                                       ctypes.c_uint64(seed & (2**64 - 1)), B, K, V, _ptr(ri),
+                                       _ptr(un), _ptr(pr), _ptr(out_ids), _ptr(out_nacc),
+                                       _ptr(row_diag), _ptr(req_diag), int(n_threads))
+    else:
+        n_bad = lib.oracle_spec_verify_rule(
+            _ptr(tl), dt, _ptr(dp), _ptr(di), _ptr(nd), _ptr(tp),
+            ctypes.c_uint64(seed & (2**64 - 1)), B, K, V, _ptr(ri), _ptr(un), _ptr(pr),
+            _ptr(out_ids), _ptr(out_nacc), _ptr(row_diag), _ptr(req_diag), int(n_threads),
+            RULE_TYPICAL, float(typical_threshold))
     if n_bad < 0:
         raise ValueError("oracle_spec_verify rejected its arguments")
     return {"out_ids": out_ids, "out_num_accepted": out_nacc, "row_diag": row_diag,

@@ -45,6 +45,14 @@
  *   - bad requests (num_draft outside [0, K], temperature NaN / negative /
  *     infinite, a draft id outside [0, V), or a sampling row whose logits are
  *     all -inf) get out_ids = -1 and out_num_accepted = -1.
+ *
+ * Typical acceptance ([P3] 验收标准, "Typical Acceptance": a draft is accepted
+ * when its probability under the target exceeds a hard threshold, and the
+ * longest such prefix is kept) is the lossy alternative rule, selected by
+ * mode ORACLE_TYPICAL: accept x_j iff p_j(x_j) > 0 and p_j(x_j) >= threshold;
+ * the token after the kept prefix (whether a draft was refused or all were
+ * kept) is drawn from p at that row by the same inverse CDF with u'.  q is not
+ * used.  Greedy requests are verified by exact match in either mode.
  */
 #include <math.h>
 #include <stdint.h>
@@ -107,6 +115,7 @@ void oracle_row_uniforms(uint64_t seed, uint64_t b, uint32_t j, double* u_accept
 /* ---------------------------------------------------------------------- */
 
 enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_LOSSLESS = 0, ORACLE_TYPICAL = 1 };
 
 static double logit_at(const void* logits, int dtype, size_t idx) {
     if (dtype == ORACLE_BF16) {
@@ -201,7 +210,8 @@ enum {
 };
 /* Per-request diagnostics (ORACLE_REQ_W doubles per b). */
 enum {
-    Q_MODE = 0,   /* -1 bad, 0 greedy, 1 residual, 2 bonus, 3 residual->p fallback */
+    Q_MODE = 0,   /* -1 bad, 0 greedy, 1 residual, 2 bonus, 3 residual->p fallback,
+                     4 typical acceptance: drawn from p at the row after the kept prefix */
     Q_NACC = 1,   /* number of accepted drafts */
     Q_EROW = 2,   /* row the emitted token came from */
     Q_UEMIT = 3,  /* emission uniform u' (sampling) */
@@ -219,7 +229,8 @@ static int verify_request(const void* logits, int dtype, const float* draft_prob
                           const int32_t* draft_ids, int n, float temperature, int b, int K,
                           int V, const double* u_accept, const double* u_emit,
                           int32_t* out_ids, int32_t* out_nacc, double* row_diag,
-                          double* req_diag, int probe, double* l, double* p, double* r) {
+                          double* req_diag, int probe, double* l, double* p, double* r,
+                          int rule, double threshold) {
     for (int j = 0; j <= K; ++j) out_ids[j] = -1;
     *out_nacc = -1;
     if (req_diag) {
@@ -268,8 +279,24 @@ static int verify_request(const void* logits, int dtype, const float* draft_prob
             break;
         }
         softmax_t(l, V, T, p);
-        const float* q = draft_probs + ((size_t)b * (size_t)K + (size_t)j) * (size_t)V;
         const double px = p[xj];
+        if (rule == ORACLE_TYPICAL) {
+            /* [P3] 验收标准, Typical Acceptance: a hard threshold on p(x_j) */
+            const int accept = (px > 0.0) && (px >= threshold);
+            if (row_diag) {
+                row_diag[j * ORACLE_ROW_W + R_PX] = px;
+                row_diag[j * ORACLE_ROW_W + R_ACCEPT] = accept;
+            }
+            if (accept) {
+                ++accepted;
+                continue;
+            }
+            erow = j;  /* the target's own token at the first refused position */
+            mode = 4;
+            emitted = inverse_cdf(p, V, u_emit[j], &mass, &lo, &hi, probe, &plo, &phi);
+            break;
+        }
+        const float* q = draft_probs + ((size_t)b * (size_t)K + (size_t)j) * (size_t)V;
         const double qx = (double)q[xj];
         const double u = u_accept[j];
         /* [P1] 保证原始分布 step 3: accept with probability min(1, p/q) */
@@ -310,7 +337,7 @@ static int verify_request(const void* logits, int dtype, const float* draft_prob
         if (greedy) {
             emitted = argmax_lowest(l, V);
         } else {
-            mode = 2;
+            mode = rule == ORACLE_TYPICAL ? 4 : 2;
             softmax_t(l, V, T, p);
             emitted = inverse_cdf(p, V, u_emit[n], &mass, &lo, &hi, probe, &plo, &phi);
         }
@@ -348,12 +375,14 @@ static int verify_request(const void* logits, int dtype, const float* draft_prob
  *   n_threads <= 0: the OpenMP default.
  * Returns the number of bad requests, or -1 on an argument error.
  */
-int oracle_spec_verify(const void* target_logits, int logits_dtype, const float* draft_probs,
-                       const int32_t* draft_ids, const int32_t* num_draft,
-                       const float* temperature, uint64_t seed, int B, int K, int V,
-                       const int64_t* req_index, const double* uniforms, const int32_t* probe,
-                       int32_t* out_ids, int32_t* out_num_accepted, double* row_diag,
-                       double* req_diag, int n_threads) {
+int oracle_spec_verify_rule(const void* target_logits, int logits_dtype,
+                            const float* draft_probs, const int32_t* draft_ids,
+                            const int32_t* num_draft, const float* temperature, uint64_t seed,
+                            int B, int K, int V, const int64_t* req_index,
+                            const double* uniforms, const int32_t* probe, int32_t* out_ids,
+                            int32_t* out_num_accepted, double* row_diag, double* req_diag,
+                            int n_threads, int rule, double threshold) {
+    if (rule != ORACLE_LOSSLESS && rule != ORACLE_TYPICAL) return -1;
     if (B < 0 || K < 0 || K > 63 || V <= 0 || !target_logits || !draft_ids || !num_draft ||
         !temperature || !out_ids || !out_num_accepted)
         return -1;
@@ -381,15 +410,17 @@ int oracle_spec_verify(const void* target_logits, int logits_dtype, const float*
                 }
             }
             int rc = -1;
-            if (draft_probs != NULL || temperature[b] == 0.0f || num_draft[b] == 0) {
-                /* greedy requests, and requests without drafts, read no q */
+            if (draft_probs != NULL || temperature[b] == 0.0f || num_draft[b] == 0 ||
+                rule == ORACLE_TYPICAL) {
+                /* greedy requests, requests without drafts and the typical rule
+                   read no q */
                 rc = verify_request(target_logits, logits_dtype, draft_probs,
                                     draft_ids + (size_t)b * (size_t)K, num_draft[b],
                                     temperature[b], b, K, V, ua, ue,
                                     out_ids + (size_t)b * (size_t)(K + 1), &out_num_accepted[b],
                                     row_diag ? row_diag + (size_t)b * (size_t)(K + 1) * ORACLE_ROW_W : NULL,
                                     req_diag ? req_diag + (size_t)b * ORACLE_REQ_W : NULL,
-                                    probe ? probe[b] : -1, l, p, r);
+                                    probe ? probe[b] : -1, l, p, r, rule, threshold);
             } else {
                 for (int j = 0; j <= K; ++j) out_ids[(size_t)b * (size_t)(K + 1) + j] = -1;
                 out_num_accepted[b] = -1;
@@ -399,6 +430,19 @@ int oracle_spec_verify(const void* target_logits, int logits_dtype, const float*
         free(scratch);
     }
     return bad;
+}
+
+/* The lossless rule (the method of the pages). */
+int oracle_spec_verify(const void* target_logits, int logits_dtype, const float* draft_probs,
+                       const int32_t* draft_ids, const int32_t* num_draft,
+                       const float* temperature, uint64_t seed, int B, int K, int V,
+                       const int64_t* req_index, const double* uniforms, const int32_t* probe,
+                       int32_t* out_ids, int32_t* out_num_accepted, double* row_diag,
+                       double* req_diag, int n_threads) {
+    return oracle_spec_verify_rule(target_logits, logits_dtype, draft_probs, draft_ids,
+                                   num_draft, temperature, seed, B, K, V, req_index, uniforms,
+                                   probe, out_ids, out_num_accepted, row_diag, req_diag,
+                                   n_threads, ORACLE_LOSSLESS, 0.0);
 }
 
 /* Philox blocks for a list of counters, for cross-checking other copies of

@@ -12,7 +12,8 @@ Sources (web pages, by title and section):
   [P2] RTP-LLM Speculative Engine 深度解析 -- 拒绝采样算法.
   [P3] 投机采样 -- 第三步..第五步, output-length cases, 调整分布 (the
        output equals sampling from p), Blockwise Parallel Decoding example,
-       验收标准 / 精确匹配.
+       验收标准 / 精确匹配, and Typical Acceptance (a hard threshold on the
+       target's probability of each draft, longest kept prefix).
 """
 from __future__ import annotations
 
@@ -490,6 +491,116 @@ def pin_lossless_closed_form(lib):
             pk = np.prod(alphas[:k]) * (1 - alphas[k] if k < K else 1.0)
             f = np.mean(a == k)
             assert abs(f - pk) < 5 * math.sqrt(pk * (1 - pk) / B) + 1e-9, (V, k, f, pk)
+
+
+# ------------------------------------------------- typical acceptance
+
+def straight_line_typical(logit_rows, draft, n, T, theta, u_emit):
+    """Independent restatement of the typical-acceptance rule ([P3] 验收标准,
+    Typical Acceptance): keep the longest prefix of drafts whose target
+    probability reaches the hard threshold; the next token is the target's
+    own draw (sampling) or argmax (greedy) at the row after the prefix."""
+    out = []
+    for j in range(n):
+        row = logit_rows[j]
+        if T == 0.0:
+            top = int(np.argmax(row))
+            if top == draft[j]:
+                out.append(draft[j])
+                continue
+            return j, out + [top]
+        p = _softmax64(row, T)
+        if p[draft[j]] > 0.0 and p[draft[j]] >= theta:
+            out.append(draft[j])
+            continue
+        return j, out + [_inv_cdf(p, u_emit[j])]
+    row = logit_rows[n]
+    if T == 0.0:
+        return n, out + [int(np.argmax(row))]
+    return n, out + [_inv_cdf(_softmax64(row, T), u_emit[n])]
+
+
+def pin_typical_brute_force(lib):
+    """Typical acceptance agrees with ``straight_line_typical`` on every draft
+    tuple of tiny vocabularies, over thresholds and a grid of uniforms; it
+    reads no draft distribution (q is not passed)."""
+    rng = np.random.default_rng(17)
+    for V, K in ((3, 3), (5, 2), (8, 1)):
+        tuples = np.array(list(itertools.product(range(V), repeat=K)), np.int32)
+        l = rng.normal(0, 1.5, (K + 1, V)).astype(np.float32)
+        l[0, V - 1] = -np.inf  # one token the target never produces
+        grid = (np.arange(8) + 0.5) / 8
+        for T in (0.0, 0.8):
+            for theta in (-1.0, 0.05, 0.2, 0.45, 2.0):
+                B = tuples.shape[0] * grid.size
+                ids = np.repeat(tuples, grid.size, 0)
+                uni = np.empty((B, K + 1, 2))
+                gi = np.tile(np.arange(grid.size), tuples.shape[0])
+                for j in range(K + 1):
+                    uni[:, j, 0] = grid[(gi + j) % grid.size]
+                    uni[:, j, 1] = grid[(gi * 3 + j) % grid.size]
+                r = _run(lib, _tile(l, B), None, ids, [K] * B, [T] * B, uniforms=uni,
+                         typical_threshold=theta)
+                assert r["n_bad"] == 0
+                lr = l.astype(np.float64).tolist()
+                T32 = float(np.float32(T))
+                for b in range(B):
+                    a, toks = straight_line_typical(lr, ids[b].tolist(), K, T32, theta,
+                                                    uni[b, :, 1].tolist())
+                    assert r["out_num_accepted"][b] == a, (V, K, T, theta, b)
+                    assert r["out_ids"][b, :a + 1].tolist() == toks, (V, K, T, theta, b)
+
+
+def pin_typical_threshold_boundary(lib):
+    """The threshold is inclusive: constant logits over V = 2^k give
+    p = 2^-k exactly, so theta = 2^-k keeps every draft and the next float
+    above it keeps none; then the emitted token is the target's own draw at
+    row 0.  A draft with p = 0 is never kept, whatever the threshold."""
+    V, K, B = 16, 3, 64
+    l = np.zeros((B, K + 1, V), np.float32)
+    ids = np.tile(np.arange(K, dtype=np.int32), (B, 1))
+    r = _run(lib, l, None, ids, [K] * B, [1.0] * B, typical_threshold=1.0 / V)
+    assert (r["out_num_accepted"] == K).all()
+    r = _run(lib, l, None, ids, [K] * B, [1.0] * B,
+             typical_threshold=float(np.nextafter(1.0 / V, 1.0)))
+    assert (r["out_num_accepted"] == 0).all()
+    assert (r["req_diag"][:, oracle.Q_EROW] == 0).all()
+    u = r["req_diag"][:, oracle.Q_UEMIT]
+    assert r["out_ids"][:, 0].tolist() == [min(V - 1, math.ceil(x * V) - 1) for x in u]
+    l2 = l.copy()
+    l2[:, 1, 1] = -np.inf
+    r = _run(lib, l2, None, ids, [K] * B, [1.0] * B, typical_threshold=-5.0)
+    assert (r["out_num_accepted"] == 1).all()
+
+
+def pin_typical_closed_form(lib):
+    """Per slot, typical acceptance keeps x_j ~ q with probability
+    sum over {x : p(x) >= theta} of q(x); the token after the kept prefix
+    follows p at its row.  Checked against 4 * 10^5 oracle trials."""
+    from scipy.stats import chisquare
+    rng = np.random.default_rng(18)
+    V, K, B = 6, 3, 400_000
+    l = rng.normal(0, 1.0, (K + 1, V)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V), K)
+    p = np.array([_softmax64(l[j].astype(np.float64).tolist(), 1.0) for j in range(K + 1)])
+    theta = float(np.median(p[:K]))
+    alphas = [q[j][p[j] >= theta].sum() for j in range(K)]
+    draw = np.empty((B, K), np.int32)
+    for j in range(K):
+        draw[:, j] = np.minimum(np.searchsorted(np.cumsum(q[j]), rng.random(B), side="right"),
+                                V - 1)
+    r = _run(lib, _tile(l, B), None, draw, [K] * B, [1.0] * B, seed=31,
+             typical_threshold=theta)
+    a = r["out_num_accepted"]
+    for k in range(K + 1):
+        pk = np.prod(alphas[:k]) * (1 - alphas[k] if k < K else 1.0)
+        f = np.mean(a == k)
+        assert abs(f - pk) < 5 * math.sqrt(pk * (1 - pk) / B) + 1e-9, (k, f, pk)
+    for j in range(K + 1):
+        sel = a == j
+        tok = r["out_ids"][sel, j]
+        obs = np.bincount(tok, minlength=V)
+        assert chisquare(obs, p[j] * sel.sum()).pvalue > 1e-3, (j, obs)
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

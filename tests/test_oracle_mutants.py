@@ -46,6 +46,15 @@ MUTANTS = {
     "negative_temperature_allowed": ("if (!(T >= 0.0) || isinf(T)) return -1;",
                                      "if (isnan(T) || isinf(T)) return -1;"),
     "empty_row_not_rejected": ("if (!finite) return -1;", "(void)finite;"),
+    "typical_threshold_strict": ("(px >= threshold)", "(px > threshold)"),
+    "typical_zero_guard_dropped": ("(px > 0.0) && (px >= threshold)", "(px >= threshold)"),
+    "typical_emission_uses_acceptance_uniform": (
+        "mode = 4;\n            emitted = inverse_cdf(p, V, u_emit[j],",
+        "mode = 4;\n            emitted = inverse_cdf(p, V, u_accept[j],"),
+    "typical_emits_from_next_row": (
+        "erow = j;  /* the target's own token at the first refused position */",
+        "erow = j;\n            if (j + 1 <= n) load_logit_row(logits, dtype, K, V, b, j + 1, l),"
+        " softmax_t(l, V, T, p);"),
 }
 
 # cheap pins first, so that most mutants are caught quickly
@@ -54,7 +63,9 @@ ORDER = ["pin_philox_kat", "pin_uniform_map", "pin_uniform_lanes", "pin_greedy_e
          "pin_bad_inputs", "pin_zero_target_prob_never_accepted", "pin_output_shape",
          "pin_softmax_vs_scipy", "pin_temperature", "pin_residual_support",
          "pin_unused_rows_ignored", "pin_request_index", "pin_equal_probs_always_accept",
-         "pin_brute_force", "pin_worked_ratio", "pin_lossless_closed_form"]
+         "pin_brute_force", "pin_worked_ratio", "pin_lossless_closed_form",
+         "pin_typical_threshold_boundary", "pin_typical_brute_force",
+         "pin_typical_closed_form"]
 
 
 def test_order_covers_all_pins():
