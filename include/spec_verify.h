@@ -129,7 +129,8 @@ spec_status spec_verify(const void* target_logits, spec_dtype logits_dtype,
  *                   {NaN, NaN, NaN, accepted}; untested rows {NaN, NaN, NaN, -1}.
  *   dbg_req         [B, 4] float32 or NULL: {mode, emission row, emission mass,
  *                   u'}; mode -1 bad, 0 greedy, 1 residual, 2 bonus,
- *                   3 residual without mass (drawn from p).
+ *                   3 residual without mass (drawn from p), 4 typical
+ *                   acceptance (drawn from p, spec_verify_typical only).
  *   dev_status      int32 device word or NULL: receives the status bits of
  *                   this call (zeroed by the call itself).
  */
@@ -140,6 +141,34 @@ spec_status spec_verify_ex(const void* target_logits, spec_dtype logits_dtype,
                            void* workspace, size_t workspace_bytes, spec_stream_t stream,
                            uint32_t request_offset, float* dbg_rows, float* dbg_req,
                            int32_t* dev_status);
+
+/*
+ * spec_verify_typical -- the lossy typical-acceptance rule ("投机采样",
+ * section 验收标准, item Typical Acceptance: a draft token is kept when the
+ * target's probability of it reaches a hard threshold, and the longest run of
+ * kept drafts is taken).
+ *
+ * Same arguments, layout, workspace and errors as spec_verify_ex, without
+ * draft_probs (the rule reads no draft distribution) and with
+ *   threshold  the hard threshold theta; NaN is SPEC_ERR_INVALID_ARG, any
+ *              other value (including +-inf) is allowed.
+ * Sampling request b: p_j = softmax(l_j / T_b) in float32 with float64
+ * accumulation; x_j is kept iff p_j(x_j) > 0 and p_j(x_j) >= theta;
+ * a_b = the number of leading kept drafts; the token at position a_b (after
+ * a refused draft, or the bonus token when all n_b are kept) is the smallest x
+ * with sum_{y<=x} p_{a_b}(y) >= u' on row a_b, u' = lane 1 of the Philox
+ * block of row a_b.  Greedy requests (T_b = 0) are verified by exact match
+ * exactly as in spec_verify.  dbg_rows give {p_j(x_j), NaN, Z_j, kept};
+ * dbg_req mode 4 for every sampling request.
+ */
+spec_status spec_verify_typical(const void* target_logits, spec_dtype logits_dtype,
+                                const int32_t* draft_ids, const int32_t* num_draft,
+                                const float* temperature, float threshold, uint64_t seed,
+                                int B, int K, int V, int32_t* out_ids,
+                                int32_t* out_num_accepted, void* workspace,
+                                size_t workspace_bytes, spec_stream_t stream,
+                                uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                                int32_t* dev_status);
 
 /*
  * spec_verify_profiled -- spec_verify with timing marks: the caller's CUDA

@@ -20,7 +20,7 @@ SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA, SPEC_ERR_WOR
 SPEC_F32, SPEC_BF16 = 0, 1
 BADBIT = {"num_draft": 1, "temperature": 2, "draft_id": 4, "empty_row": 8, "no_probs": 16,
           "timeout": 32}
-MODE_BAD, MODE_GREEDY, MODE_RESIDUAL, MODE_BONUS, MODE_FALLBACK = -1, 0, 1, 2, 3
+MODE_BAD, MODE_GREEDY, MODE_RESIDUAL, MODE_BONUS, MODE_FALLBACK, MODE_TYPICAL = -1, 0, 1, 2, 3, 4
 MAX_K = 31
 KERNELS = ("k_plan", "k_row_stats", "k_sample", "k_emit")  # launch order
 N_KERNELS = len(KERNELS)
@@ -49,6 +49,9 @@ def _declare(lib):
     lib.spec_verify.argtypes = common
     lib.spec_verify_ex.restype = i32
     lib.spec_verify_ex.argtypes = common + [u32, vp, vp, vp]
+    lib.spec_verify_typical.restype = i32
+    lib.spec_verify_typical.argtypes = [vp, i32, vp, vp, vp, ctypes.c_float, u64, i32, i32, i32,
+                                        vp, vp, vp, sz, vp, u32, vp, vp, vp]
     lib.spec_verify_profiled.restype = i32
     lib.spec_verify_profiled.argtypes = common + [vp]
     lib.spec_verify_host_small_bytes.restype = sz
@@ -175,6 +178,61 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
                 _p(out_num_accepted), _p(workspace), workspace.numel(), st)
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify")
+    if debug:
+        return out_ids, out_num_accepted, dbg_rows, dbg_req
+    return out_ids, out_num_accepted
+
+
+def spec_verify_typical(target_logits: torch.Tensor, draft_ids: torch.Tensor,
+                        num_draft: torch.Tensor, temperature: torch.Tensor, threshold: float,
+                        seed: int, *, out_ids: torch.Tensor | None = None,
+                        out_num_accepted: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, stream=None,
+                        request_offset: int = 0, debug: bool = False,
+                        dev_status: torch.Tensor | None = None):
+    """Typical-acceptance verification on the GPU (include/spec_verify.h,
+    spec_verify_typical): drafts are kept while p_j(x_j) >= threshold.
+
+    Returns (out_ids, out_num_accepted), plus (dbg_rows, dbg_req) when debug=True.
+    """
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, K+1, V]")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    dev = target_logits.device
+    if target_logits.dtype == torch.bfloat16:
+        dt = SPEC_BF16
+    elif target_logits.dtype == torch.float32:
+        dt = SPEC_F32
+    else:
+        raise ValueError("target_logits must be bfloat16 or float32")
+    _check(target_logits, "target_logits", target_logits.dtype)
+    _check(draft_ids, "draft_ids", torch.int32, (B, K), dev)
+    _check(num_draft, "num_draft", torch.int32, (B,), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    if out_ids is None:
+        out_ids = torch.empty((B, K1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _check(out_ids, "out_ids", torch.int32, (B, K1), dev)
+    _check(out_num_accepted, "out_num_accepted", torch.int32, (B,), dev)
+    if workspace is None:
+        workspace = new_workspace(B, K, V, dev)
+    dbg_rows = dbg_req = None
+    if debug:
+        dbg_rows = torch.empty((B, K1, 4), dtype=torch.float32, device=dev)
+        dbg_req = torch.empty((B, 4), dtype=torch.float32, device=dev)
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, (1,), dev)
+    with torch.cuda.device(dev):
+        rc = lib().spec_verify_typical(
+            _p(target_logits), dt, _p(draft_ids), _p(num_draft), _p(temperature),
+            ctypes.c_float(threshold), ctypes.c_uint64(seed & (2**64 - 1)), B, K, V,
+            _p(out_ids), _p(out_num_accepted), _p(workspace), workspace.numel(),
+            _stream(stream), ctypes.c_uint32(request_offset & 0xFFFFFFFF), _p(dbg_rows),
+            _p(dbg_req), _p(dev_status))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify_typical")
     if debug:
         return out_ids, out_num_accepted, dbg_rows, dbg_req
     return out_ids, out_num_accepted

@@ -18,6 +18,9 @@
 //   4. write the accepted prefix and the -1 tail; greedy requests also write
 //      the emitted token (argmax of row a_b); sampling requests are queued for
 //      k_sample (residual at row a_b < n_b, bonus at row a_b == n_b).
+// Under the typical-acceptance rule ("投机采样" 验收标准, Typical Acceptance)
+// step 2 keeps x_j iff p > 0 and p >= the call's threshold (no q, no u_j) and
+// every sampling request is queued as a draw from p at row a_b.
 // Values written by other warps during the same kernel (partials, gathered
 // logits) are read through L2 (ld.global.cg), after the caller's fence.
 #pragma once
@@ -88,6 +91,7 @@ __device__ __noinline__ void accept_request(const Params& P, int b) {
     const int x = draft_lane ? P.ids[(size_t)b * P.K + lane] : -1;
     float2 g = make_float2(0.f, 0.f);
     if (draft_lane && !greedy) g = __ldcg(P.gath + (size_t)b * K1 + lane);
+    const bool typical = P.rule == RULE_TYPICAL;
     uint4 rb = make_uint4(0, 0, 0, 0);
     if (!greedy && lane <= n) rb = row_block(P, b, lane);
 
@@ -198,10 +202,16 @@ __device__ __noinline__ void accept_request(const Params& P, int b) {
         } else {
             const float lx = g.x, qx = g.y;
             p = __fdiv_rn(exp2f(weight_arg(lx, my_m, offset_of(my_m, kappa), kappa)), my_Z);
-            u = uniform01(rb.x);
-            // u <= p / q  <=>  u q <= p (q > 0); the product of two floats is
-            // exact in double, so the comparison takes no rounding
-            acc = (p > 0.f) && (qx == 0.f || double(u) * double(qx) <= double(p));
+            if (typical) {
+                // "投机采样" 验收标准, Typical Acceptance: a hard threshold on
+                // the target's probability of the draft
+                acc = (p > 0.f) && (p >= P.threshold);
+            } else {
+                u = uniform01(rb.x);
+                // u <= p / q  <=>  u q <= p (q > 0); the product of two floats
+                // is exact in double, so the comparison takes no rounding
+                acc = (p > 0.f) && (qx == 0.f || double(u) * double(qx) <= double(p));
+            }
         }
     }
 
@@ -218,14 +228,17 @@ __device__ __noinline__ void accept_request(const Params& P, int b) {
     if (lane == 0) P.out_nacc[b] = a;
     if (!greedy && lane == a) {
         ReqRec r;
-        r.mode = a < n ? MODE_RESIDUAL : MODE_BONUS;
+        // typical acceptance draws the next token from p at row a, refused
+        // draft or not: it joins the bonus queue
+        const bool resid = a < n && !typical;
+        r.mode = typical ? MODE_TYPICAL : (resid ? MODE_RESIDUAL : MODE_BONUS);
         r.erow = a;
         r.m = my_m;
         r.kappa = kappa;
         r.Z = double(my_Z);
         r.u2 = uniform01(rb.y);
         r.b = b;
-        if (a < n) {
+        if (resid) {
             const int i = atomicAdd(&P.hdr[HDR_NRES], 1);
             P.res_rec[i] = r;
         } else {

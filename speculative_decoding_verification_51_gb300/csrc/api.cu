@@ -120,8 +120,10 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
                            int B, int K, int V, int32_t* out_ids, int32_t* out_num_accepted,
                            void* workspace, size_t workspace_bytes, spec_stream_t stream,
                            uint32_t request_offset, float* dbg_rows, float* dbg_req,
-                           int32_t* dev_status, cudaEvent_t* events) {
+                           int32_t* dev_status, cudaEvent_t* events, int rule = RULE_LOSSLESS,
+                           float threshold = 0.f) {
     if (!sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
+    if (rule == RULE_TYPICAL && threshold != threshold) return SPEC_ERR_INVALID_ARG;
     if (logits_dtype != SPEC_F32 && logits_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
     if (V % 8 != 0) return SPEC_ERR_UNSUPPORTED;
     if (B == 0) return SPEC_OK;
@@ -160,6 +162,8 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     P.cnt = at<int>(workspace, L.cnt);
     P.seed = seed;
     P.req_off = request_offset;
+    P.rule = rule;
+    P.threshold = threshold;
     P.dtype = logits_dtype;
     P.B = B;
     P.K = K;
@@ -231,6 +235,19 @@ spec_status spec_verify_ex(const void* target_logits, spec_dtype logits_dtype,
                        temperature, seed, B, K, V, out_ids, out_num_accepted, workspace,
                        workspace_bytes, stream, request_offset, dbg_rows, dbg_req, dev_status,
                        nullptr);
+}
+
+spec_status spec_verify_typical(const void* target_logits, spec_dtype logits_dtype,
+                                const int32_t* draft_ids, const int32_t* num_draft,
+                                const float* temperature, float threshold, uint64_t seed, int B,
+                                int K, int V, int32_t* out_ids, int32_t* out_num_accepted,
+                                void* workspace, size_t workspace_bytes, spec_stream_t stream,
+                                uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                                int32_t* dev_status) {
+    return verify_impl(target_logits, logits_dtype, nullptr, draft_ids, num_draft, temperature,
+                       seed, B, K, V, out_ids, out_num_accepted, workspace, workspace_bytes,
+                       stream, request_offset, dbg_rows, dbg_req, dev_status, nullptr,
+                       RULE_TYPICAL, threshold);
 }
 
 spec_status spec_verify_profiled(const void* target_logits, spec_dtype logits_dtype,

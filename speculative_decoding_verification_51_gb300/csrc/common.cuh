@@ -48,7 +48,11 @@ constexpr int SAMPLE_WARPS = SV_SAMPLE_WARPS;  // warps per k_sample CTA (2 stag
 constexpr int PLAN_THREADS = 1024;
 
 enum { HDR_ROWS = 0, HDR_NRES = 1, HDR_NBONUS = 2, HDR_STATUS = 3, HDR_INTS = 64 };
-enum { MODE_BAD = -1, MODE_GREEDY = 0, MODE_RESIDUAL = 1, MODE_BONUS = 2, MODE_FALLBACK = 3 };
+enum { MODE_BAD = -1, MODE_GREEDY = 0, MODE_RESIDUAL = 1, MODE_BONUS = 2, MODE_FALLBACK = 3,
+       MODE_TYPICAL = 4 };
+// acceptance rule of a call: the lossless test u <= p / q, or typical
+// acceptance (p >= a hard threshold, no draft distribution)
+enum { RULE_LOSSLESS = 0, RULE_TYPICAL = 1 };
 
 // Per (row, chunk) statistics written by k_row_stats.
 struct __align__(16) Partial {
@@ -91,6 +95,8 @@ struct Params {
     int* cnt;         // [B] (row, chunk) tiles of each request finished so far
     uint64_t seed;
     uint32_t req_off;
+    int rule;         // RULE_*
+    float threshold;  // typical acceptance: keep x_j iff p_j(x_j) >= threshold
     int dtype;  // SPEC_F32 / SPEC_BF16
     int B, K, K1, V;
     int C;   // ceil(V / TILE): chunks per row

@@ -33,7 +33,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_plan(Params P) {
             int flags = 0;
             if (n < 0 || n > P.K) flags |= SPEC_BADBIT_NUM_DRAFT;
             if (!(T >= 0.f) || T > FLT_MAX) flags |= SPEC_BADBIT_TEMPERATURE;
-            if (!flags && T > 0.f && n > 0 && P.probs == nullptr) flags |= SPEC_BADBIT_NO_PROBS;
+            if (!flags && T > 0.f && n > 0 && P.probs == nullptr && P.rule == RULE_LOSSLESS)
+                flags |= SPEC_BADBIT_NO_PROBS;
             rows = flags ? 0 : n + 1;
             P.req_flags[b] = flags;
             P.cnt[b] = 0;

@@ -177,7 +177,7 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
     float qx = 0.f;  // q_j(x_j), fetched at row start by the warp that owns x_j's tile
     auto prefetch_q = [&]() {
         const long long t_x = cr * P.C + rc.xchunk;
-        if (rc.xj >= 0 && t_x >= t0 && t_x < t1 && lane == 0) {
+        if (P.rule == RULE_LOSSLESS && rc.xj >= 0 && t_x >= t0 && t_x < t1 && lane == 0) {
             const int b = rc.slot / P.K1, j = rc.slot - b * P.K1;
             qx = __ldg(P.probs + ((size_t)b * P.K + j) * P.V + rc.xj);
         }

@@ -473,7 +473,10 @@ __device__ __forceinline__ void emit_body(const Params& P) {
         if (k < n_res)
             emit_residual<DT>(P, P.res_rec[k], int(k), ws, 0);
         else
-            emit_from_p<DT>(P, P.bonus_rec[k - n_res], MODE_BONUS, ws, 0);
+            {
+            const ReqRec& r = P.bonus_rec[k - n_res];
+            emit_from_p<DT>(P, r, r.mode, ws, 0);
+        }
     }
     finish_stages(P, ws);
 }

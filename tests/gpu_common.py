@@ -50,6 +50,26 @@ def check_parity(w: W.Workload, tag: str, **kw) -> parity.Report:
     return rep
 
 
+def run_gpu_typical(w: W.Workload, threshold: float, debug=True, **kw):
+    ensure_built()
+    res = binding.spec_verify_typical(w.target_logits, w.draft_ids, w.num_draft, w.temperature,
+                                      threshold, w.seed, debug=debug, **kw)
+    torch.cuda.synchronize()
+    return [None if t is None else t.cpu().numpy() for t in res]
+
+
+def check_parity_typical(w: W.Workload, threshold: float, tag: str, **kw):
+    """Typical acceptance on the GPU against the oracle's typical rule; the
+    draft distribution is not passed to either side."""
+    inputs = W.to_numpy(w)
+    inputs["draft_probs"] = None
+    ids, nacc, rows, req = run_gpu_typical(w, threshold, **kw)
+    ref = oracle.spec_verify(**inputs, typical_threshold=threshold)
+    rep = parity.compare(inputs, ids, nacc, rows, ref, typical_threshold=threshold)
+    print(f"[{tag}] {rep.summary()}")
+    return rep, (ids, nacc, rows, req), ref
+
+
 def custom_workload(logits: np.ndarray, probs: np.ndarray | None, ids, num, temp, *,
                     bf16: bool, seed: int = 0, device="cuda") -> W.Workload:
     """A workload from explicit host arrays (logits as float values)."""

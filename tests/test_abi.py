@@ -80,3 +80,20 @@ def test_host_side_errors(lib):
     assert lib.spec_status_str(4) == b"SPEC_ERR_WORKSPACE"
     assert lib.spec_verify_status_ptr(ctypes.c_void_p(0x1000)) == 0x100C
     assert bd.host_small_bytes(3, 2) == 5 * 256
+
+
+def test_typical_host_side_errors(lib):
+    """spec_verify_typical rejects a NaN threshold and bad sizes on the host."""
+    from speculative_decoding_verification_51_gb300 import binding as bd
+    vp = ctypes.c_void_p
+
+    def call(theta, B=2, K=3, V=64, ws=0x80000):
+        return lib.spec_verify_typical(vp(0x10000), 1, vp(0x30000), vp(0x40000), vp(0x50000),
+                                       ctypes.c_float(theta), ctypes.c_uint64(0), B, K, V,
+                                       vp(0x60000), vp(0x70000), vp(ws), 1 << 30, vp(0),
+                                       ctypes.c_uint32(0), None, None, None)
+    assert call(float("nan")) == bd.SPEC_ERR_INVALID_ARG
+    assert call(0.1, K=32) == bd.SPEC_ERR_INVALID_ARG
+    assert call(0.1, V=1020) == bd.SPEC_ERR_UNSUPPORTED
+    assert call(0.1, B=0) == bd.SPEC_OK
+    assert call(float("inf"), ws=0x80010) == bd.SPEC_ERR_WORKSPACE
