@@ -68,6 +68,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_spec_verify_rule.argtypes = [vp, i32, vp, vp, vp, vp, u64, i32, i32, i32,
                                             vp, vp, vp, vp, vp, vp, vp, i32, i32,
                                             ctypes.c_double]
+    lib.oracle_tree_verify.restype = i32
+    lib.oracle_tree_verify.argtypes = [vp, i32, vp, vp, vp, vp, vp, u64, i32, i32, i32,
+                                       vp, vp, vp, vp, vp, vp, vp, vp, i32]
     lib.oracle_philox_blocks.restype = None
     lib.oracle_philox_blocks.argtypes = [vp, vp, i64, vp]
     lib.oracle_row_uniforms.restype = None
@@ -151,6 +154,58 @@ def spec_verify(target_logits: np.ndarray, draft_probs: np.ndarray | None,
         raise ValueError("oracle_spec_verify rejected its arguments")
     return {"out_ids": out_ids, "out_num_accepted": out_nacc, "row_diag": row_diag,
             "req_diag": req_diag, "n_bad": int(n_bad)}
+
+
+def tree_verify(target_logits: np.ndarray, draft_probs: np.ndarray | None,
+                tree_tokens: np.ndarray, tree_parents: np.ndarray, num_nodes: np.ndarray,
+                temperature: np.ndarray, seed: int, *, logits_dtype: str | None = None,
+                req_index: np.ndarray | None = None, uniforms: np.ndarray | None = None,
+                probe: np.ndarray | None = None, n_threads: int = 0, lib=None) -> dict:
+    """Token-tree verification by the oracle.
+
+    target_logits: [B, N, V] float32, or uint16 bf16 bit patterns (row v: the
+    target's logits for the token after node v).  draft_probs [B, N, V]
+    float32 (row c: the distribution node c's token was drawn from; row 0
+    unused) or None.  tree_tokens / tree_parents [B, N] int32 (node 0 is the
+    root), num_nodes [B], temperature [B].
+    uniforms: None (Philox) or [B, N, 2]: lane 0 of entry c - 1 is child c's
+    acceptance uniform, lane 1 of entry v node v's emission uniform.
+    """
+    lib = lib or load()
+    tl = np.ascontiguousarray(target_logits)
+    if logits_dtype is None:
+        logits_dtype = "bf16" if tl.dtype == np.uint16 else "f32"
+    if logits_dtype == "bf16":
+        assert tl.dtype in (np.uint16, np.int16), tl.dtype
+        dt = 1
+    else:
+        tl = np.ascontiguousarray(tl, dtype=np.float32)
+        dt = 0
+    B, N, V = tl.shape
+    dp = None if draft_probs is None else np.ascontiguousarray(draft_probs, dtype=np.float32)
+    if dp is not None:
+        assert dp.shape == (B, N, V), (dp.shape, (B, N, V))
+    tt = np.ascontiguousarray(tree_tokens, dtype=np.int32).reshape(B, N)
+    tpar = np.ascontiguousarray(tree_parents, dtype=np.int32).reshape(B, N)
+    nn = np.ascontiguousarray(num_nodes, dtype=np.int32).reshape(B)
+    tp = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
+    ri = None if req_index is None else np.ascontiguousarray(req_index, dtype=np.int64).reshape(B)
+    un = None if uniforms is None else np.ascontiguousarray(uniforms, dtype=np.float64).reshape(B, N, 2)
+    pr = None if probe is None else np.ascontiguousarray(probe, dtype=np.int32).reshape(B)
+    out_ids = np.empty((B, N), dtype=np.int32)
+    out_nacc = np.empty((B,), dtype=np.int32)
+    out_last = np.empty((B,), dtype=np.int32)
+    node_diag = np.empty((B, N, ROW_W), dtype=np.float64)
+    req_diag = np.empty((B, REQ_W), dtype=np.float64)
+    n_bad = lib.oracle_tree_verify(_ptr(tl), dt, _ptr(dp), _ptr(tt), _ptr(tpar), _ptr(nn),
+                                   _ptr(tp), ctypes.c_uint64(seed & (2**64 - 1)), B, N, V,
+                                   _ptr(ri), _ptr(un), _ptr(pr), _ptr(out_ids), _ptr(out_nacc),
+                                   _ptr(out_last), _ptr(node_diag), _ptr(req_diag),
+                                   int(n_threads))
+    if n_bad < 0:
+        raise ValueError("oracle_tree_verify rejected its arguments")
+    return {"out_ids": out_ids, "out_num_accepted": out_nacc, "out_last_node": out_last,
+            "node_diag": node_diag, "req_diag": req_diag, "n_bad": int(n_bad)}
 
 
 def philox_blocks(ctrs: np.ndarray, key: tuple[int, int], lib=None) -> np.ndarray:

@@ -445,6 +445,228 @@ int oracle_spec_verify(const void* target_logits, int logits_dtype, const float*
                                    n_threads, ORACLE_LOSSLESS, 0.0);
 }
 
+/* ---------------------------------------------------------------------- */
+/* Token-tree verification.                                                */
+/* ---------------------------------------------------------------------- */
+
+/* Row v of a [B, N, V] logits array into dst[V] (float64). */
+static void load_node_row(const void* logits, int dtype, int N, int V, int b, int v,
+                          double* dst) {
+    size_t base = ((size_t)b * (size_t)N + (size_t)v) * (size_t)V;
+    for (int x = 0; x < V; ++x) dst[x] = logit_at(logits, dtype, base + (size_t)x);
+}
+
+/*
+ * One request of token-tree verification ([P3] 验证方案: the candidate
+ * sequences share prefixes in a trie, and the target scores every node in one
+ * pass; the verifier walks the trie from the root).  Node 0 is the root (the
+ * accepted context); node c >= 1 carries token tok[c] and parent par[c] < c.
+ * Row v of the logits is the target's distribution of the token after node
+ * v's prefix; row c of q the draft distribution tok[c] was drawn from.
+ *   greedy (T == 0, [P3] 精确匹配): at node v, the first child (in index
+ *     order) whose token is the argmax of row v is accepted; else the argmax
+ *     is emitted.
+ *   sampling: the children of v are tested in index order against a running
+ *     target r (r = p_v first): child c is accepted with probability
+ *     min(1, r(x)/q_c(x)); after a rejection r becomes
+ *     norm(max(0, r - q_c)) (kept as it was if that has no mass).  When no
+ *     child is accepted the token is drawn from the last residual (from r if
+ *     it had no mass, from p_v at a node without children).
+ * ua[c] is the acceptance uniform of child c, ue[v] the emission uniform of
+ * node v.  out[0..a-1] are the tokens of the accepted path, out[a] the
+ * emitted token.  Returns 0, or -1 for a bad request.
+ */
+static int verify_tree_request(const void* logits, int dtype, const float* draft_probs,
+                               const int32_t* tok, const int32_t* par, int n, float temperature,
+                               int b, int N, int V, const double* ua, const double* ue,
+                               int32_t* out, int32_t* out_nacc, int32_t* out_last,
+                               double* node_diag, double* req_diag, int probe, double* l,
+                               double* r, double* w) {
+    for (int c = 0; c < N; ++c) out[c] = -1;
+    *out_nacc = -1;
+    *out_last = -1;
+    if (node_diag)
+        for (int c = 0; c < N; ++c) {
+            for (int k = 0; k < ORACLE_ROW_W; ++k) node_diag[c * ORACLE_ROW_W + k] = NAN;
+            node_diag[c * ORACLE_ROW_W + R_ACCEPT] = -1;
+        }
+    if (req_diag) {
+        for (int k = 0; k < ORACLE_REQ_W; ++k) req_diag[k] = NAN;
+        req_diag[Q_MODE] = -1;
+    }
+    const double T = (double)temperature;
+    if (n < 1 || n > N) return -1;
+    if (isnan(T) || T < 0.0 || isinf(T)) return -1;
+    for (int c = 1; c < n; ++c) {
+        if (par[c] < 0 || par[c] >= c) return -1;
+        if (tok[c] < 0 || tok[c] >= V) return -1;
+    }
+    const int greedy = (T == 0.0);
+    if (!greedy) {
+        if (n > 1 && draft_probs == NULL) return -1;
+        for (int v = 0; v < n; ++v) { /* every node row needs a finite logit */
+            load_node_row(logits, dtype, N, V, b, v, l);
+            int finite = 0;
+            for (int x = 0; x < V; ++x)
+                if (l[x] > -INFINITY) finite = 1;
+            if (finite == 0) return -1;
+        }
+    }
+
+    int v = 0, depth = 0, emitted = -1, mode = greedy ? 0 : 2;
+    double mass = NAN, lo = NAN, hi = NAN, plo = NAN, phi = NAN;
+    for (;;) {
+        load_node_row(logits, dtype, N, V, b, v, l);
+        if (greedy) {
+            const int g = argmax_lowest(l, V);
+            int next = -1;
+            for (int c = v + 1; c < n && next < 0; ++c)
+                if (par[c] == v) {
+                    if (node_diag) node_diag[c * ORACLE_ROW_W + R_ACCEPT] = tok[c] == g;
+                    if (tok[c] == g) next = c;
+                }
+            if (next < 0) {
+                emitted = g;
+                break;
+            }
+            out[depth++] = tok[next];
+            v = next;
+            continue;
+        }
+        softmax_t(l, V, T, r); /* the running target starts at p_v */
+        const double* emit_w = r;
+        int has_child = 0, next = -1;
+        mode = 2;
+        for (int c = v + 1; c < n; ++c) {
+            if (par[c] != v) continue;
+            has_child = 1;
+            const float* q = draft_probs + ((size_t)b * (size_t)N + (size_t)c) * (size_t)V;
+            const int x = tok[c];
+            const double rx = r[x], qx = (double)q[x], u = ua[c];
+            const int accept = (rx > 0.0) && (qx == 0.0 || u <= rx / qx);
+            if (node_diag) {
+                node_diag[c * ORACLE_ROW_W + R_PX] = rx;
+                node_diag[c * ORACLE_ROW_W + R_QX] = qx;
+                node_diag[c * ORACLE_ROW_W + R_U] = u;
+                node_diag[c * ORACLE_ROW_W + R_ACCEPT] = accept;
+            }
+            if (accept) {
+                next = c;
+                break;
+            }
+            /* rejected: the residual max(0, r - q_c) */
+            double S = 0.0;
+            for (int y = 0; y < V; ++y) {
+                const double e = r[y] - (double)q[y];
+                w[y] = e > 0.0 ? e : 0.0;
+                S += w[y];
+            }
+            if (S > 0.0) {
+                emit_w = w; /* unnormalised: the inverse CDF normalises */
+                mode = 1;
+                int more = 0; /* a later sibling tests against the normalised residual */
+                for (int c2 = c + 1; c2 < n; ++c2)
+                    if (par[c2] == v) more = 1;
+                if (more)
+                    for (int y = 0; y < V; ++y) r[y] = w[y] / S;
+            } else {
+                emit_w = r; /* no residual mass: r stays */
+                mode = 3;
+            }
+        }
+        if (next >= 0) {
+            out[depth++] = tok[next];
+            v = next;
+            continue;
+        }
+        if (!has_child) mode = 2;
+        emitted = inverse_cdf(emit_w, V, ue[v], &mass, &lo, &hi, probe, &plo, &phi);
+        break;
+    }
+    out[depth] = emitted;
+    *out_nacc = depth;
+    *out_last = v;
+    if (req_diag) {
+        req_diag[Q_MODE] = mode;
+        req_diag[Q_NACC] = depth;
+        req_diag[Q_EROW] = v;
+        req_diag[Q_UEMIT] = greedy ? NAN : ue[v];
+        req_diag[Q_MASS] = mass;
+        req_diag[Q_LO] = lo;
+        req_diag[Q_HI] = hi;
+        req_diag[Q_PLO] = plo;
+        req_diag[Q_PHI] = phi;
+    }
+    return 0;
+}
+
+/*
+ * Token-tree verification over a batch.
+ *   target_logits [B, N, V]; draft_probs [B, N, V] f32 (row 0 unused; may be
+ *   NULL if no sampling request has a child); tree_tokens [B, N] and
+ *   tree_parents [B, N] (entries of node 0 unused); num_nodes [B] in [1, N];
+ *   temperature [B].
+ *   uniforms: NULL -> Philox(seed, req_index[b] (or b), ...): child c's
+ *             acceptance uniform is lane 0 of block (b, c - 1), node v's
+ *             emission uniform lane 1 of block (b, v); else [B, N, 2] doubles
+ *             (lane 0 of entry c - 1 for child c, lane 1 of entry v for v).
+ *   out_ids [B, N], out_num_accepted [B], out_last_node [B]; node_diag
+ *   [B, N, ORACLE_ROW_W] (per child c: r(x), q_c(x), u, accepted) and req_diag
+ *   [B, ORACLE_REQ_W] may be NULL.
+ * Returns the number of bad requests, or -1 on an argument error.
+ */
+int oracle_tree_verify(const void* target_logits, int logits_dtype, const float* draft_probs,
+                       const int32_t* tree_tokens, const int32_t* tree_parents,
+                       const int32_t* num_nodes, const float* temperature, uint64_t seed, int B,
+                       int N, int V, const int64_t* req_index, const double* uniforms,
+                       const int32_t* probe, int32_t* out_ids, int32_t* out_num_accepted,
+                       int32_t* out_last_node, double* node_diag, double* req_diag,
+                       int n_threads) {
+    if (B < 0 || N < 1 || N > 64 || V <= 0 || !target_logits || !tree_tokens ||
+        !tree_parents || !num_nodes || !temperature || !out_ids || !out_num_accepted ||
+        !out_last_node)
+        return -1;
+    if (logits_dtype != ORACLE_F32 && logits_dtype != ORACLE_BF16) return -1;
+    int bad = 0;
+#ifdef _OPENMP
+    if (n_threads <= 0) n_threads = omp_get_max_threads();
+#pragma omp parallel num_threads(n_threads) reduction(+ : bad)
+#endif
+    {
+        double* scratch = (double*)malloc(sizeof(double) * 3 * (size_t)V);
+        double *l = scratch, *r = scratch + V, *w = scratch + 2 * (size_t)V;
+        double ua[64], ue[64];
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int b = 0; b < B; ++b) {
+            const uint64_t gb = req_index ? (uint64_t)req_index[b] : (uint64_t)b;
+            for (int v = 0; v < N; ++v) {
+                double a0, e0;
+                if (uniforms) {
+                    a0 = uniforms[((size_t)b * (size_t)N + (size_t)v) * 2 + 0];
+                    e0 = uniforms[((size_t)b * (size_t)N + (size_t)v) * 2 + 1];
+                } else {
+                    oracle_row_uniforms(seed, gb, (uint32_t)v, &a0, &e0);
+                }
+                ue[v] = e0;
+                if (v + 1 < 64) ua[v + 1] = a0; /* block (b, v) lane 0 -> child v + 1 */
+            }
+            ua[0] = NAN;
+            const int rc = verify_tree_request(
+                target_logits, logits_dtype, draft_probs, tree_tokens + (size_t)b * (size_t)N,
+                tree_parents + (size_t)b * (size_t)N, num_nodes[b], temperature[b], b, N, V, ua,
+                ue, out_ids + (size_t)b * (size_t)N, &out_num_accepted[b], &out_last_node[b],
+                node_diag ? node_diag + (size_t)b * (size_t)N * ORACLE_ROW_W : NULL,
+                req_diag ? req_diag + (size_t)b * ORACLE_REQ_W : NULL, probe ? probe[b] : -1, l,
+                r, w);
+            if (rc != 0) ++bad;
+        }
+        free(scratch);
+    }
+    return bad;
+}
+
 /* Philox blocks for a list of counters, for cross-checking other copies of
  * the generator: out[4*i..4*i+3] = Philox(key, ctr[4*i..4*i+3]). */
 void oracle_philox_blocks(const uint32_t* ctrs, const uint32_t key[2], int64_t n, uint32_t* out) {

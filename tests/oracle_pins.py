@@ -603,4 +603,192 @@ def pin_typical_closed_form(lib):
         assert chisquare(obs, p[j] * sel.sum()).pvalue > 1e-3, (j, obs)
 
 
+# ------------------------------------------------- token-tree verification
+
+def _run_tree(lib, logits, q, tok, par, n, T, seed=0, **kw):
+    logits = np.asarray(logits, dtype=np.float32)
+    B, N, V = logits.shape
+    q = None if q is None else np.asarray(q, dtype=np.float32).reshape(B, N, V)
+    return oracle.tree_verify(logits, q, np.asarray(tok, np.int32).reshape(B, N),
+                              np.asarray(par, np.int32).reshape(B, N),
+                              np.asarray(n, np.int32).reshape(B),
+                              np.asarray(T, np.float32).reshape(B), seed, lib=lib, **kw)
+
+
+def _children(par, n, v):
+    return [c for c in range(v + 1, n) if par[c] == v]
+
+
+def straight_line_tree(rows, q, tok, par, n, T, ua, ue):
+    """Independent restatement of the tree walk ([P3] 验证方案, token tree
+    verification; residual chain over siblings) for tiny trees: returns
+    (accepted tokens, emitted token, last node)."""
+    v, path = 0, []
+    while True:
+        kids = _children(par, n, v)
+        if T == 0.0:
+            g = int(np.argmax(rows[v]))
+            hit = [c for c in kids if tok[c] == g]
+            if not hit:
+                return path, g, v
+            path.append(tok[hit[0]])
+            v = hit[0]
+            continue
+        r = np.array(_softmax64(list(rows[v]), T))
+        emit = r
+        nxt = None
+        for i, c in enumerate(kids):
+            qc = np.asarray(q[c], dtype=np.float64)
+            x = tok[c]
+            if r[x] > 0 and (qc[x] == 0 or ua[c] <= r[x] / qc[x]):
+                nxt = c
+                break
+            res = np.maximum(r - qc, 0.0)
+            if res.sum() > 0:
+                emit = res
+                if i + 1 < len(kids):
+                    r = res / res.sum()
+            else:
+                emit = r
+        if nxt is not None:
+            path.append(tok[nxt])
+            v = nxt
+            continue
+        return path, _inv_cdf(list(emit), ue[v]), v
+
+
+def _random_tree(rng, N, n):
+    par = np.full(N, -1, np.int32)
+    for c in range(1, n):
+        par[c] = rng.integers(0, c)
+    return par
+
+
+def pin_tree_chain_is_chain(lib):
+    """A trie whose every node has one child is a chain of drafts: tree
+    verification then returns exactly what the chain verifier returns (same
+    Philox blocks, same rules), for greedy and sampling rows, bonus, residual
+    and zero-residual cases."""
+    rng = np.random.default_rng(19)
+    B, K, V = 64, 4, 24
+    l = rng.normal(0, 1.5, (B, K + 1, V)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V) * 0.5, (B, K)).astype(np.float32)
+    q[::7] *= 3.0  # unnormalised q: residuals without mass occur
+    ids = np.array([[rng.choice(V, p=q[b, j] / q[b, j].sum()) for j in range(K)] for b in range(B)],
+                   np.int32)
+    ids[::5] = l[::5, :K].argmax(-1)  # long accepted prefixes
+    n = rng.integers(0, K + 1, B).astype(np.int32)
+    T = np.where(rng.random(B) < 0.3, 0.0, rng.uniform(0.5, 1.5, B)).astype(np.float32)
+    chain = _run(lib, l, q, ids, n, T, seed=77)
+    tq = np.zeros((B, K + 1, V), np.float32)
+    tq[:, 1:] = q
+    tok = np.zeros((B, K + 1), np.int32)
+    tok[:, 1:] = ids
+    par = np.tile(np.arange(-1, K, dtype=np.int32), (B, 1))
+    tree = _run_tree(lib, l, tq, tok, par, n + 1, T, seed=77)
+    assert np.array_equal(tree["out_num_accepted"], chain["out_num_accepted"])
+    assert np.array_equal(tree["out_ids"], chain["out_ids"])
+    assert np.array_equal(tree["out_last_node"], chain["out_num_accepted"])
+
+
+def pin_tree_brute_force(lib):
+    """Agreement with ``straight_line_tree`` on many random tiny tries (with
+    repeated sibling tokens), greedy and sampling, over a grid of uniforms."""
+    rng = np.random.default_rng(20)
+    for V, N in ((3, 6), (5, 7), (8, 5)):
+        B = 300
+        l = rng.normal(0, 1.2, (B, N, V)).astype(np.float32)
+        q = rng.dirichlet(np.ones(V) * 0.8, (B, N)).astype(np.float32)
+        tok = rng.integers(0, V, (B, N)).astype(np.int32)
+        par = np.stack([_random_tree(rng, N, N) for _ in range(B)])
+        n = rng.integers(1, N + 1, B).astype(np.int32)
+        T = np.where(rng.random(B) < 0.35, 0.0, rng.uniform(0.6, 1.4, B)).astype(np.float32)
+        uni = rng.random((B, N, 2)) * 0.999 + 0.0005
+        r = _run_tree(lib, l, q, tok, par, n, T, uniforms=uni)
+        assert r["n_bad"] == 0
+        for b in range(B):
+            ua = {c: uni[b, c - 1, 0] for c in range(1, N)}
+            ue = uni[b, :, 1]
+            path, e, v = straight_line_tree(l[b].astype(np.float64), q[b], tok[b].tolist(),
+                                            par[b].tolist(), int(n[b]), float(T[b]), ua, ue)
+            a = int(r["out_num_accepted"][b])
+            assert a == len(path), (V, N, b)
+            assert r["out_ids"][b, :a].tolist() == path, (V, N, b)
+            assert int(r["out_ids"][b, a]) == e, (V, N, b)
+            assert int(r["out_last_node"][b]) == v, (V, N, b)
+
+
+def pin_tree_first_token_law(lib):
+    """Children drawn independently from q and tested along the residual
+    chain leave the first token of the output distributed as the target's p
+    at the root (chi-square over 4 * 10^5 tries of a root with three
+    children), and the first child is kept with probability sum min(p, q)."""
+    from scipy.stats import chisquare
+    rng = np.random.default_rng(21)
+    V, N, B = 6, 4, 400_000
+    l = rng.normal(0, 1.0, (N, V)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V)).astype(np.float32)
+    qd = q.astype(np.float64)
+    p = np.array(_softmax64(l[0].astype(np.float64).tolist(), 1.0))
+    cdf = np.cumsum(qd / qd.sum())
+    tok = np.zeros((B, N), np.int32)
+    for c in range(1, N):
+        tok[:, c] = np.minimum(np.searchsorted(cdf, rng.random(B), side="right"), V - 1)
+    par = np.tile(np.array([-1, 0, 0, 0], np.int32), (B, 1))
+    r = _run_tree(lib, _tile(l, B), _tile(np.tile(q, (N, 1)), B), tok, par, np.full(B, N),
+                  np.ones(B), seed=41)
+    first = r["out_ids"][:, 0]
+    obs = np.bincount(first, minlength=V)
+    assert chisquare(obs, p * B).pvalue > 1e-3, obs
+    kept1 = np.mean((r["out_num_accepted"] == 1) & (r["out_last_node"] == 1))
+    alpha = np.minimum(p, qd / qd.sum()).sum()
+    assert abs(kept1 - alpha) < 5 * math.sqrt(alpha * (1 - alpha) / B), (kept1, alpha)
+
+
+def pin_tree_bad_inputs(lib):
+    """Malformed tries give -1 outputs and are counted; good requests are not
+    affected: a parent at or after its child, a token outside [0, V), a node
+    count outside [1, N], a negative temperature, children without q."""
+    V, N = 8, 4
+    l = np.zeros((6, N, V), np.float32)
+    q = np.full((6, N, V), 1.0 / V, np.float32)
+    tok = np.ones((6, N), np.int32)
+    par = np.tile(np.array([-1, 0, 1, 2], np.int32), (6, 1))
+    n = np.full(6, N, np.int32)
+    T = np.ones(6, np.float32)
+    par[1, 2] = 2          # parent not before the child
+    tok[2, 3] = V          # token out of range
+    n[3] = 0               # no root
+    T[4] = -1.0            # bad temperature
+    r = _run_tree(lib, l, q, tok, par, n, T)
+    assert r["n_bad"] == 4
+    assert (r["out_num_accepted"][1:5] == -1).all() and (r["out_ids"][1:5] == -1).all()
+    assert r["out_num_accepted"][0] >= 0 and r["out_num_accepted"][5] >= 0
+    r2 = _run_tree(lib, l[:1], None, tok[:1], par[:1], n[:1], T[:1])
+    assert r2["n_bad"] == 1  # sampling children without their q
+
+
+def pin_tree_unused_nodes_ignored(lib):
+    """Nodes at or beyond num_nodes are never read: poisoning their logits,
+    tokens, parents and q changes nothing."""
+    rng = np.random.default_rng(22)
+    B, N, V = 40, 6, 10
+    l = rng.normal(0, 1, (B, N, V)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V), (B, N)).astype(np.float32)
+    tok = rng.integers(0, V, (B, N)).astype(np.int32)
+    par = np.stack([_random_tree(rng, N, N) for _ in range(B)])
+    n = rng.integers(1, N, B).astype(np.int32)
+    T = np.where(rng.random(B) < 0.4, 0.0, 1.0).astype(np.float32)
+    a = _run_tree(lib, l, q, tok, par, n, T, seed=3)
+    l2, q2, tok2, par2 = l.copy(), q.copy(), tok.copy(), par.copy()
+    for b in range(B):
+        l2[b, n[b]:] = np.nan
+        q2[b, n[b]:] = np.nan
+        tok2[b, n[b]:] = -7
+        par2[b, n[b]:] = 99
+    c = _run_tree(lib, l2, q2, tok2, par2, n, T, seed=3)
+    assert np.array_equal(a["out_ids"], c["out_ids"])
+    assert np.array_equal(a["out_num_accepted"], c["out_num_accepted"])
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -51,6 +51,14 @@ MUTANTS = {
     "typical_emission_uses_acceptance_uniform": (
         "mode = 4;\n            emitted = inverse_cdf(p, V, u_emit[j],",
         "mode = 4;\n            emitted = inverse_cdf(p, V, u_accept[j],"),
+    "tree_residual_not_renormalised": ("for (int y = 0; y < V; ++y) r[y] = w[y] / S;",
+                                       "for (int y = 0; y < V; ++y) r[y] = w[y];"),
+    "tree_child_uniform_shifted": ("if (v + 1 < 64) ua[v + 1] = a0;", "if (v < 64) ua[v] = a0;"),
+    "tree_greedy_last_matching_child": ("for (int c = v + 1; c < n && next < 0; ++c)",
+                                        "for (int c = v + 1; c < n; ++c)"),
+    "tree_emits_from_running_target": ("emit_w = w; /* unnormalised", "emit_w = r; /* unnormalised"),
+    "tree_parent_order_unchecked": ("if (par[c] < 0 || par[c] >= c) return -1;",
+                                    "if (par[c] < 0) return -1;"),
     "typical_emits_from_next_row": (
         "erow = j;  /* the target's own token at the first refused position */",
         "erow = j;\n            if (j + 1 <= n) load_logit_row(logits, dtype, K, V, b, j + 1, l),"
@@ -65,7 +73,8 @@ ORDER = ["pin_philox_kat", "pin_uniform_map", "pin_uniform_lanes", "pin_greedy_e
          "pin_unused_rows_ignored", "pin_request_index", "pin_equal_probs_always_accept",
          "pin_brute_force", "pin_worked_ratio", "pin_lossless_closed_form",
          "pin_typical_threshold_boundary", "pin_typical_brute_force",
-         "pin_typical_closed_form"]
+         "pin_typical_closed_form", "pin_tree_bad_inputs", "pin_tree_unused_nodes_ignored",
+         "pin_tree_chain_is_chain", "pin_tree_brute_force", "pin_tree_first_token_law"]
 
 
 def test_order_covers_all_pins():
