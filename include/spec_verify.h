@@ -62,6 +62,7 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 #define SPEC_BADBIT_EMPTY_ROW 8u   /* a sampling row j <= num_draft[b] whose logits are all -inf */
 #define SPEC_BADBIT_NO_PROBS 16u   /* a sampling request with drafts but draft_probs == NULL */
 #define SPEC_BADBIT_TIMEOUT 32u    /* an internal bounded wait gave up (never expected) */
+#define SPEC_BADBIT_TREE 64u       /* spec_verify_tree: a node whose parent is not an earlier node */
 
 /* Human-readable name of a status code (static string). */
 const char* spec_status_str(spec_status s);
@@ -169,6 +170,56 @@ spec_status spec_verify_typical(const void* target_logits, spec_dtype logits_dty
                                 size_t workspace_bytes, spec_stream_t stream,
                                 uint32_t request_offset, float* dbg_rows, float* dbg_req,
                                 int32_t* dev_status);
+
+/*
+ * spec_verify_tree -- token-tree verification ("投机采样", section 验证方案:
+ * candidate draft sequences that share a prefix are merged into a trie, and
+ * the target scores every node in one pass; SpecInfer's token-tree verifier).
+ *
+ * Per request b the trie has n_b = num_nodes[b] nodes, 1 <= n_b <= N <= 32;
+ * node 0 is the accepted context (the root), node c >= 1 carries the draft
+ * token tree_tokens[b, c] and the parent tree_parents[b, c], an earlier node
+ * (0 <= parent < c).  Entries of node 0 and of nodes >= n_b are ignored.
+ *   target_logits [B, N, V] f32 | bf16, 16-byte aligned: row v = the target's
+ *                 logits of the token that follows node v's prefix.
+ *   draft_probs   [B, N, V] f32 or NULL: row c = the draft distribution node
+ *                 c's token was drawn from (row 0 unused).  NULL is allowed
+ *                 when no sampling request has a child.
+ *   tree_tokens, tree_parents [B, N] int32; num_nodes [B] int32;
+ *   temperature   [B] f32: 0 = greedy, > 0 sampling.
+ *   out_ids       [B, N] int32 (written): the tokens of the accepted path
+ *                 (root excluded), then the emitted token, then -1.
+ *   out_num_accepted [B] (written): the path length a_b, or -1 (bad request).
+ *   out_last_node [B] (written): the last accepted node (0: none), or -1.
+ * Greedy (T = 0, exact match): from v = 0, the first child of v (in node
+ * index order) whose token is the lowest-index argmax of row v is accepted;
+ * else that argmax is emitted.  Sampling: the children of v are tested in
+ * index order against a running target r, r = p_v = softmax(l_v / T) first:
+ * child c is kept iff r(x_c) > 0 and (q_c(x_c) == 0 or u_c <= r(x_c) /
+ * q_c(x_c)); after a rejection r becomes max(0, r - q_c) normalised (kept as
+ * it was if that has no mass).  When no child is kept the emitted token is the
+ * smallest x whose prefix sum of the last residual (of r if it had no mass,
+ * of p_v at a node without children) reaches u' times its total.  u_c is lane
+ * 0 of the Philox block of row c - 1 and u' lane 1 of the block of row v
+ * (rows as in spec_verify, request index b + request_offset), so a trie with
+ * one child per node gives exactly the result of spec_verify on the chain.
+ * Workspace: spec_verify_tree_workspace_size(B, N, V) bytes, 256-byte
+ * aligned.  Errors as spec_verify_ex; a node whose parent is not an earlier
+ * node sets SPEC_BADBIT_TREE, a token outside [0, V) SPEC_BADBIT_DRAFT_ID,
+ * num_nodes outside [1, N] SPEC_BADBIT_NUM_DRAFT.  dbg_nodes [B, N, 4] (per
+ * tested child c: {r(x_c), u_c, q_c(x_c), kept}; greedy: {NaN, NaN, NaN,
+ * kept}) and dbg_req [B, 4] ({mode, last node, emission mass, u'}) may be
+ * NULL.  N > 32 is SPEC_ERR_UNSUPPORTED.
+ */
+size_t spec_verify_tree_workspace_size(int B, int N, int V);
+spec_status spec_verify_tree(const void* target_logits, spec_dtype logits_dtype,
+                             const float* draft_probs, const int32_t* tree_tokens,
+                             const int32_t* tree_parents, const int32_t* num_nodes,
+                             const float* temperature, uint64_t seed, int B, int N, int V,
+                             int32_t* out_ids, int32_t* out_num_accepted,
+                             int32_t* out_last_node, void* workspace, size_t workspace_bytes,
+                             spec_stream_t stream, uint32_t request_offset, float* dbg_nodes,
+                             float* dbg_req, int32_t* dev_status);
 
 /*
  * spec_verify_profiled -- spec_verify with timing marks: the caller's CUDA

@@ -19,7 +19,7 @@ from . import build as _build
 SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA, SPEC_ERR_WORKSPACE = range(5)
 SPEC_F32, SPEC_BF16 = 0, 1
 BADBIT = {"num_draft": 1, "temperature": 2, "draft_id": 4, "empty_row": 8, "no_probs": 16,
-          "timeout": 32}
+          "timeout": 32, "tree": 64}
 MODE_BAD, MODE_GREEDY, MODE_RESIDUAL, MODE_BONUS, MODE_FALLBACK, MODE_TYPICAL = -1, 0, 1, 2, 3, 4
 MAX_K = 31
 KERNELS = ("k_plan", "k_row_stats", "k_sample", "k_emit")  # launch order
@@ -49,6 +49,11 @@ def _declare(lib):
     lib.spec_verify.argtypes = common
     lib.spec_verify_ex.restype = i32
     lib.spec_verify_ex.argtypes = common + [u32, vp, vp, vp]
+    lib.spec_verify_tree_workspace_size.restype = sz
+    lib.spec_verify_tree_workspace_size.argtypes = [i32, i32, i32]
+    lib.spec_verify_tree.restype = i32
+    lib.spec_verify_tree.argtypes = [vp, i32, vp, vp, vp, vp, vp, u64, i32, i32, i32, vp, vp, vp,
+                                     vp, sz, vp, u32, vp, vp, vp]
     lib.spec_verify_typical.restype = i32
     lib.spec_verify_typical.argtypes = [vp, i32, vp, vp, vp, ctypes.c_float, u64, i32, i32, i32,
                                         vp, vp, vp, sz, vp, u32, vp, vp, vp]
@@ -236,6 +241,59 @@ def spec_verify_typical(target_logits: torch.Tensor, draft_ids: torch.Tensor,
     if debug:
         return out_ids, out_num_accepted, dbg_rows, dbg_req
     return out_ids, out_num_accepted
+
+
+def spec_verify_tree(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
+                     tree_tokens: torch.Tensor, tree_parents: torch.Tensor,
+                     num_nodes: torch.Tensor, temperature: torch.Tensor, seed: int, *,
+                     workspace: torch.Tensor | None = None, stream=None, request_offset: int = 0,
+                     debug: bool = False, dev_status: torch.Tensor | None = None):
+    """Token-tree verification on the GPU (include/spec_verify.h,
+    spec_verify_tree).  Returns (out_ids [B, N], out_num_accepted [B],
+    out_last_node [B]), plus (dbg_nodes [B, N, 4], dbg_req [B, 4]) when debug."""
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, N, V]")
+    B, N, V = target_logits.shape
+    dev = target_logits.device
+    if target_logits.dtype == torch.bfloat16:
+        dt = SPEC_BF16
+    elif target_logits.dtype == torch.float32:
+        dt = SPEC_F32
+    else:
+        raise ValueError("target_logits must be bfloat16 or float32")
+    _check(target_logits, "target_logits", target_logits.dtype)
+    if draft_probs is not None:
+        _check(draft_probs, "draft_probs", torch.float32, (B, N, V), dev)
+    _check(tree_tokens, "tree_tokens", torch.int32, (B, N), dev)
+    _check(tree_parents, "tree_parents", torch.int32, (B, N), dev)
+    _check(num_nodes, "num_nodes", torch.int32, (B,), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    out_ids = torch.empty((B, N), dtype=torch.int32, device=dev)
+    out_nacc = torch.empty((B,), dtype=torch.int32, device=dev)
+    out_last = torch.empty((B,), dtype=torch.int32, device=dev)
+    if workspace is None:
+        n = int(lib().spec_verify_tree_workspace_size(B, N, V))
+        if n == 0:
+            raise ValueError("unsupported tree size")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    dbg_nodes = dbg_req = None
+    if debug:
+        dbg_nodes = torch.empty((B, N, 4), dtype=torch.float32, device=dev)
+        dbg_req = torch.empty((B, 4), dtype=torch.float32, device=dev)
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, (1,), dev)
+    with torch.cuda.device(dev):
+        rc = lib().spec_verify_tree(
+            _p(target_logits), dt, _p(draft_probs), _p(tree_tokens), _p(tree_parents),
+            _p(num_nodes), _p(temperature), ctypes.c_uint64(seed & (2**64 - 1)), B, N, V,
+            _p(out_ids), _p(out_nacc), _p(out_last), _p(workspace), workspace.numel(),
+            _stream(stream), ctypes.c_uint32(request_offset & 0xFFFFFFFF), _p(dbg_nodes),
+            _p(dbg_req), _p(dev_status))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify_tree")
+    if debug:
+        return out_ids, out_nacc, out_last, dbg_nodes, dbg_req
+    return out_ids, out_nacc, out_last
 
 
 def spec_verify_profiled(target_logits, draft_probs, draft_ids, num_draft, temperature, seed,

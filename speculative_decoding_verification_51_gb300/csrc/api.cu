@@ -121,7 +121,9 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
                            void* workspace, size_t workspace_bytes, spec_stream_t stream,
                            uint32_t request_offset, float* dbg_rows, float* dbg_req,
                            int32_t* dev_status, cudaEvent_t* events, int rule = RULE_LOSSLESS,
-                           float threshold = 0.f) {
+                           float threshold = 0.f, const int32_t* parents = nullptr,
+                           int32_t* out_last = nullptr) {
+    const bool tree = parents != nullptr;
     if (!sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
     if (rule == RULE_TYPICAL && threshold != threshold) return SPEC_ERR_INVALID_ARG;
     if (logits_dtype != SPEC_F32 && logits_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
@@ -160,6 +162,10 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     P.rsum = at<float>(workspace, L.rsum);
     P.gath = at<float2>(workspace, L.gath);
     P.cnt = at<int>(workspace, L.cnt);
+    P.tree = tree ? 1 : 0;
+    P.parents = parents;
+    P.out_last = out_last;
+    P.tmass = at<float>(workspace, L.tmass);
     P.seed = seed;
     P.req_off = request_offset;
     P.rule = rule;
@@ -191,6 +197,12 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
         e = launch(bf16 ? k_row_stats_bf16 : k_row_stats_f32, unsigned(g1),
                    STATS_WARPS * 32, stats_smem(logits_dtype), st, true, P);
     if (e == cudaSuccess) e = mark(2);
+    if (tree) {  // the walks, one CTA per request
+        if (e == cudaSuccess)
+            e = launch(bf16 ? k_tree_walk_bf16 : k_tree_walk_f32, unsigned(B), TREE_THREADS, 0,
+                       st, false, P);
+        return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    }
     if (e == cudaSuccess)
         e = launch(bf16 ? k_sample_bf16 : k_sample_f32, unsigned(g3), SAMPLE_WARPS * 32,
                    sample_smem(logits_dtype), st, true, P);
@@ -248,6 +260,28 @@ spec_status spec_verify_typical(const void* target_logits, spec_dtype logits_dty
                        seed, B, K, V, out_ids, out_num_accepted, workspace, workspace_bytes,
                        stream, request_offset, dbg_rows, dbg_req, dev_status, nullptr,
                        RULE_TYPICAL, threshold);
+}
+
+size_t spec_verify_tree_workspace_size(int B, int N, int V) {
+    if (N < 1 || N > TREE_MAX_NODES) return 0;
+    return spec_verify_workspace_size(B, N - 1, V);
+}
+
+spec_status spec_verify_tree(const void* target_logits, spec_dtype logits_dtype,
+                             const float* draft_probs, const int32_t* tree_tokens,
+                             const int32_t* tree_parents, const int32_t* num_nodes,
+                             const float* temperature, uint64_t seed, int B, int N, int V,
+                             int32_t* out_ids, int32_t* out_num_accepted,
+                             int32_t* out_last_node, void* workspace, size_t workspace_bytes,
+                             spec_stream_t stream, uint32_t request_offset, float* dbg_nodes,
+                             float* dbg_req, int32_t* dev_status) {
+    if (N < 1) return SPEC_ERR_INVALID_ARG;
+    if (N > TREE_MAX_NODES) return SPEC_ERR_UNSUPPORTED;
+    if (B > 0 && (!tree_tokens || !tree_parents || !out_last_node)) return SPEC_ERR_INVALID_ARG;
+    return verify_impl(target_logits, logits_dtype, draft_probs, tree_tokens, num_nodes,
+                       temperature, seed, B, N - 1, V, out_ids, out_num_accepted, workspace,
+                       workspace_bytes, stream, request_offset, dbg_nodes, dbg_req, dev_status,
+                       nullptr, RULE_LOSSLESS, 0.f, tree_parents, out_last_node);
 }
 
 spec_status spec_verify_profiled(const void* target_logits, spec_dtype logits_dtype,

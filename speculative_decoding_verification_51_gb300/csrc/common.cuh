@@ -93,6 +93,12 @@ struct Params {
     float* rsum;      // [B*C] residual chunk sums (TILE-token chunks)
     float2* gath;     // [B*(K+1)] {l_j(x_j), q_j(x_j)} gathered by k_row_stats
     int* cnt;         // [B] (row, chunk) tiles of each request finished so far
+    // token-tree verification (tree != 0): row v of request b is node v, row c
+    // of probs the draft distribution of node c; parents[b * K1 + c] < c
+    int tree;
+    const int32_t* parents;  // [B, N] (N = K1)
+    int32_t* out_last;       // [B] last accepted node
+    float* tmass;            // [B, C] per-chunk masses of a tree walk's residual
     uint64_t seed;
     uint32_t req_off;
     int rule;         // RULE_*
@@ -104,7 +110,7 @@ struct Params {
 
 // Workspace layout (byte offsets, each section 256-byte aligned).
 struct Layout {
-    size_t hdr, rowlist, req_flags, part, res_rec, bonus_rec, rsum, gath, cnt, total;
+    size_t hdr, rowlist, req_flags, part, res_rec, bonus_rec, rsum, gath, cnt, tmass, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -122,6 +128,7 @@ inline Layout make_layout(int B, int K, int V) {
     L.rsum = o;       o = align256(o + size_t(B) * C * sizeof(float));
     L.gath = o;       o = align256(o + size_t(B) * K1 * sizeof(float2));
     L.cnt = o;        o = align256(o + size_t(B) * sizeof(int));
+    L.tmass = o;      o = align256(o + size_t(B) * C * sizeof(float));
     L.total = o;
     return L;
 }
@@ -322,6 +329,11 @@ __global__ void k_sample_f32(Params P);
 __global__ void k_sample_bf16(Params P);
 __global__ void k_emit_f32(Params P);
 __global__ void k_emit_bf16(Params P);
+
+__global__ void k_tree_walk_f32(Params P);
+__global__ void k_tree_walk_bf16(Params P);
+constexpr int TREE_THREADS = 256;
+constexpr int TREE_MAX_NODES = 32;
 
 __global__ void k_philox_fill(uint64_t seed, const uint32_t* ctrs, int64_t n, uint32_t* out);
 

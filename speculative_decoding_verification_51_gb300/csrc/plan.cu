@@ -33,15 +33,24 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_plan(Params P) {
             int flags = 0;
             if (n < 0 || n > P.K) flags |= SPEC_BADBIT_NUM_DRAFT;
             if (!(T >= 0.f) || T > FLT_MAX) flags |= SPEC_BADBIT_TEMPERATURE;
-            if (!flags && T > 0.f && n > 0 && P.probs == nullptr && P.rule == RULE_LOSSLESS)
+            if (P.tree) {  // n counts the nodes, the root included
+                flags = 0;
+                if (n < 1 || n > P.K1) flags |= SPEC_BADBIT_NUM_DRAFT;
+                if (!(T >= 0.f) || T > FLT_MAX) flags |= SPEC_BADBIT_TEMPERATURE;
+                if (!flags && T > 0.f && n > 1 && P.probs == nullptr)
+                    flags |= SPEC_BADBIT_NO_PROBS;
+            } else if (!flags && T > 0.f && n > 0 && P.probs == nullptr &&
+                       P.rule == RULE_LOSSLESS) {
                 flags |= SPEC_BADBIT_NO_PROBS;
-            rows = flags ? 0 : n + 1;
+            }
+            rows = flags ? 0 : (P.tree ? n : n + 1);
             P.req_flags[b] = flags;
             P.cnt[b] = 0;
             flags_any |= flags;
             if (flags) {  // no row of a bad request is read: its outputs are final here
                 for (int j = 0; j < P.K1; ++j) P.out_ids[(size_t)b * P.K1 + j] = -1;
                 P.out_nacc[b] = -1;
+                if (P.out_last) P.out_last[b] = -1;
                 const float NaN = __int_as_float(0x7fc00000);
                 if (P.dbg_rows)
                     for (int j = 0; j < P.K1; ++j) {

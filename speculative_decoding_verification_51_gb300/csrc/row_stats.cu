@@ -111,7 +111,7 @@ __device__ __forceinline__ RowCtx row_ctx(const Params& P, long long r) {
     rc.greedy = (T == 0.f);
     rc.kappa = rc.greedy ? 0.f : kappa_of(T);
     int x = -1;
-    if (!rc.greedy && j < rc.n) {
+    if (!P.tree && !rc.greedy && j < rc.n) {  // tree requests gather nothing here
         x = P.ids[(size_t)b * P.K + j];
         if (x < 0 || x >= P.V) x = -1;  // reported by the acceptance step
     }
@@ -188,7 +188,7 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
     int seg_b = rc.b, seg_n = rc.n, seg_tiles = 0;
     auto flush = [&]() {
         int last = 0;
-        if (lane == 0 && seg_tiles > 0) {
+        if (lane == 0 && seg_tiles > 0 && !P.tree) {  // trees are walked by k_tree_walk
             __threadfence();  // this warp's partials before its count
             const int total = (seg_n + 1) * P.C;
             last = atomicAdd(&P.cnt[seg_b], seg_tiles) + seg_tiles == total;
