@@ -60,6 +60,12 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--mode", choices=["chain", "typical", "tree"], default="chain",
+                    help="chain: the lossless / greedy verifier (the headline line); "
+                         "typical: typical acceptance on the same workload; tree: "
+                         "token-tree verification of tries with --tree-nodes nodes")
+    ap.add_argument("--threshold", type=float, default=0.01, help="typical acceptance threshold")
+    ap.add_argument("--tree-nodes", type=int, default=16)
     return ap.parse_args()
 
 
@@ -270,11 +276,115 @@ def cpu_baseline(w, budget_s):
                       f"repetitions, {sec * 1e3:.1f} ms each"}
 
 
+def run_variant(args, rank, world, local):
+    """Device time per call of the typical-acceptance or token-tree verifier
+    (L2 flushed before every call, CUDA events on the call's stream)."""
+    from speculative_decoding_verification_51_gb300 import binding
+    from speculative_decoding_verification_51_gb300 import build as _build
+    from speculative_decoding_verification_51_gb300 import workloads as W
+    from speculative_decoding_verification_51_gb300 import sharding
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+    binding.lib()
+    spec = W.SPECS[args.config]
+    esz = 2 if spec.dtype == "bf16" else 4
+    if args.mode == "typical":
+        w = W.make_workload(args.config, device=dev)
+        B, K, V = w.B, w.K, w.V
+        offset = sharding.weak_offset(rank, B)
+        pos = W.positions(w.num_draft)
+        ws = binding.new_workspace(B, K, V, dev)
+        out_ids = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+        out_nacc = torch.empty((B,), dtype=torch.int32, device=dev)
+        rows = W.valid_rows(w.num_draft)
+        algo = rows * V * esz + B * (K * 4 + 8) + B * ((K + 1) * 4 + 4)
+
+        def step(seed):
+            binding.spec_verify_typical(w.target_logits, w.draft_ids, w.num_draft, w.temperature,
+                                        args.threshold, seed, out_ids=out_ids,
+                                        out_num_accepted=out_nacc, workspace=ws,
+                                        request_offset=offset)
+        wname = (f"config{args.config} ({spec.description}), typical acceptance, "
+                 f"threshold {args.threshold}")
+    else:
+        N = args.tree_nodes
+        tw = W.make_tree_workload(spec.B, N, spec.V, bf16=spec.dtype == "bf16",
+                                  seed=args.config, device=dev)
+        B, V = spec.B, spec.V
+        offset = sharding.weak_offset(rank, B)
+        pos = int((tw.nodes.long() - 1).sum())
+        ws = torch.empty(binding.lib().spec_verify_tree_workspace_size(B, N, V),
+                         dtype=torch.uint8, device=dev)
+        rows = int(tw.nodes.long().sum())
+        algo = rows * V * esz + B * N * 8 + B * (N * 4 + 8)  # every node row once; lower bound
+
+        def step(seed):
+            binding.spec_verify_tree(tw.logits, tw.probs, tw.tokens, tw.parents, tw.nodes,
+                                     tw.temp, seed, workspace=ws, request_offset=offset)
+        wname = (f"token trees: B={B} tries of up to {N} nodes (num_nodes ~ U{{1..{N}}}), "
+                 f"V={V} {spec.dtype} logits, 30% greedy")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def flush_l2(i):
+        flush.fill_(i & 0xFF)
+        flush_rd.sum()
+
+    for i in range(args.warmup):
+        flush_l2(i)
+        step(1000 + i)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        for i in range(args.steps):
+            flush_l2(i + 7)
+            evs[i][0].record(stream)
+            step(2000 + i)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    ms = sharding.max_over_ranks(ms, device=dev)
+    peak, peak_kind, _ = measured_peak()
+    gbs = algo / (ms * 1e-3) / 1e9
+    n_kernels = 3 if args.mode == "tree" else 4
+    line = {
+        "metric": METRIC, "value": world * pos / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "mode": args.mode,
+        "config": {"workload": wname, "positions_per_step": pos,
+                   "l2": "flushed before every timed call: 256 MiB write, then 256 MiB read"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None, "kernel": "whole call",
+                     "algorithmic_bytes_per_launch": algo, "peak_kind": peak_kind},
+        "gpu_launches": n_kernels * args.steps, "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.mode != "chain":
+        run_variant(args, rank, world, local)
         return
 
     from speculative_decoding_verification_51_gb300 import binding

@@ -14,74 +14,12 @@ from __future__ import annotations
 from dataclasses import dataclass, field
 
 import numpy as np
-import torch
 
 import oracle
+from speculative_decoding_verification_51_gb300.workloads import (  # noqa: F401
+    TreeWorkload, make_tree_workload, random_parents)
 
 TIE = 1e-6
-
-
-@dataclass
-class TreeWorkload:
-    logits: torch.Tensor   # [B, N, V] f32 | bf16 (cuda)
-    probs: torch.Tensor    # [B, N, V] f32
-    tokens: torch.Tensor   # [B, N] int32
-    parents: torch.Tensor  # [B, N] int32
-    nodes: torch.Tensor    # [B] int32
-    temp: torch.Tensor     # [B] f32
-    seed: int
-
-    def to_numpy(self) -> dict:
-        tl = self.logits.detach().cpu()
-        tl_np = tl.view(torch.int16).numpy().view("uint16") if tl.dtype == torch.bfloat16 \
-            else tl.numpy()
-        return {"target_logits": tl_np, "draft_probs": self.probs.cpu().numpy(),
-                "tree_tokens": self.tokens.cpu().numpy(), "tree_parents": self.parents.cpu().numpy(),
-                "num_nodes": self.nodes.cpu().numpy(), "temperature": self.temp.cpu().numpy(),
-                "seed": self.seed}
-
-
-def random_parents(rng, B: int, N: int, width: float) -> np.ndarray:
-    """Tries whose node c picks its parent among the earlier nodes; `width`
-    in (0, 1] biases towards recent nodes (deep, narrow) when small."""
-    par = np.full((B, N), -1, np.int32)
-    for c in range(1, N):
-        lo = np.maximum(0, c - np.maximum(1, (width * c)).astype(int))
-        par[:, c] = rng.integers(lo, c)
-    return par
-
-
-def make_tree_workload(B, N, V, *, bf16=True, seed=0, greedy_frac=0.3, width=0.6,
-                       noise=1.0, device="cuda") -> TreeWorkload:
-    """Zipf-like target logits per node, drafts drawn from a noisy copy of the
-    parent's distribution (so that many are accepted), random tries."""
-    g = torch.Generator(device="cpu").manual_seed(seed)
-    rng = np.random.default_rng(seed)
-    rank = torch.arange(1, V + 1, dtype=torch.float32)
-    base = -1.1 * torch.log(rank)
-    perm = torch.argsort(torch.rand(B, N, V, generator=g), dim=-1)
-    logits = base[perm] + torch.randn(B, N, V, generator=g)
-    par = random_parents(rng, B, N, width)
-    T = torch.from_numpy(np.where(rng.random(B) < greedy_frac, 0.0,
-                                  rng.uniform(0.5, 1.3, B)).astype(np.float32))
-    # draft distribution of node c: a noisy copy of its parent's target row
-    pl = logits[torch.arange(B)[:, None], torch.from_numpy(par.clip(min=0)).long()]
-    dlog = pl + noise * torch.randn(B, N, V, generator=g)
-    Tq = torch.where(T > 0, T, torch.ones_like(T))[:, None, None]
-    q = torch.softmax(dlog / Tq, dim=-1)
-    tok = torch.multinomial(q.reshape(B * N, V), 1, generator=g).reshape(B, N).to(torch.int32)
-    # greedy requests: a child often repeats the parent's argmax
-    am = logits.argmax(-1)
-    for b in np.nonzero(T.numpy() == 0)[0]:
-        for c in range(1, N):
-            if rng.random() < 0.5:
-                tok[b, c] = int(am[b, par[b, c]])
-    tok[:, 0] = 0
-    nodes = torch.from_numpy(rng.integers(1, N + 1, B).astype(np.int32))
-    lt = logits.to(torch.bfloat16) if bf16 else logits
-    return TreeWorkload(lt.to(device).contiguous(), q.to(device).contiguous(),
-                        tok.to(device).contiguous(), torch.from_numpy(par).to(device).contiguous(),
-                        nodes.to(device), T.to(device), seed * 7919 + 13)
 
 
 @dataclass
