@@ -435,7 +435,29 @@ def main():
         step(1000 + i)
     torch.cuda.synchronize()
 
-    # ---- timed region: K calls, device time per call, L2 flushed before each
+    # One call captured in a CUDA graph, the seed read from device memory: a
+    # step writes its seed, then replays the four kernels of the call.
+    seed_buf = torch.zeros(1, dtype=torch.int64, device=dev)
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
+                            w.temperature, 0, out_ids=out_ids, out_num_accepted=out_nacc,
+                            workspace=ws, request_offset=offset, seed_dev=seed_buf, stream=cap)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
+                            w.temperature, 0, out_ids=out_ids, out_num_accepted=out_nacc,
+                            workspace=ws, request_offset=offset, seed_dev=seed_buf, stream=cap)
+    torch.cuda.synchronize()
+    for i in range(args.warmup):
+        flush_l2(i)
+        seed_buf.fill_(1500 + i)
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, device time per step, L2 flushed before each
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     if world > 1:
@@ -444,8 +466,9 @@ def main():
     with ClockSampler(dev) as clk:
         for i in range(args.steps):
             flush_l2(i + 7)
+            seed_buf.fill_(2000 + i)
             evs[i][0].record(stream)
-            step(2000 + i)
+            graph.replay()
             evs[i][1].record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -454,6 +477,19 @@ def main():
     ms = sum(step_ms) / len(step_ms)
     ms = sharding.max_over_ranks(ms, device=dev)
     clocks = clk.summary()
+
+    # the same calls launched directly (no graph), for comparison
+    n_direct = min(args.steps, 50)
+    devs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n_direct)]
+    torch.cuda.synchronize()
+    for i in range(n_direct):
+        flush_l2(i + 5)
+        devs[i][0].record(stream)
+        step(2500 + i)
+        devs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms_direct = statistics.mean(a.elapsed_time(b) for a, b in devs)
 
     # ---- per-kernel durations (same workload, marks between the kernels)
     n_prof = min(args.steps, 50)
@@ -528,7 +564,11 @@ def main():
                    "logits_dtype": str(w.target_logits.dtype).replace("torch.", ""),
                    "positions_per_step": pos, "rows_per_step": W.valid_rows(w.num_draft),
                    "l2": "flushed before every timed call: 256 MiB write, then 256 MiB read "
-                         "(L2 left full of clean unrelated lines)"},
+                         "(L2 left full of clean unrelated lines)",
+                   "launch": "one spec_verify call captured in a CUDA graph (seed read from "
+                             "device memory, written before each replay); ms_per_step_direct: "
+                             "the same call launched directly"},
+        "ms_per_step_direct": round(ms_direct, 5),
         "hbm_gbs_step": round(step_gbs, 1), "hbm_frac_step": round(step_gbs / peak, 4),
         "kernels_ms": {n: round(t, 5) for n, t in zip(names, kern_ms)},
         "accept_rate": float(nacc_cpu.clamp(min=0).sum()) / max(1, pos),

@@ -172,6 +172,25 @@ spec_status spec_verify_typical(const void* target_logits, spec_dtype logits_dty
                                 int32_t* dev_status);
 
 /*
+ * spec_verify_dev_seed -- spec_verify_ex with the Philox seed read from
+ * device memory (*seed_dev, 8-byte aligned) when the kernels run instead of
+ * passed by value.  A call enqueues a fixed sequence of kernels, allocates
+ * nothing and never synchronises, so it can be captured once in a CUDA graph
+ * and replayed for every decoding step, the caller writing the step's seed to
+ * *seed_dev before each replay; replaying saves the launch gaps between the
+ * kernels.  The pages have no counterpart to this entry point.  A NULL or
+ * misaligned seed_dev is SPEC_ERR_INVALID_ARG; otherwise as spec_verify_ex.
+ */
+spec_status spec_verify_dev_seed(const void* target_logits, spec_dtype logits_dtype,
+                                 const float* draft_probs, const int32_t* draft_ids,
+                                 const int32_t* num_draft, const float* temperature,
+                                 const uint64_t* seed_dev, int B, int K, int V, int32_t* out_ids,
+                                 int32_t* out_num_accepted, void* workspace,
+                                 size_t workspace_bytes, spec_stream_t stream,
+                                 uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                                 int32_t* dev_status);
+
+/*
  * spec_verify_tree -- token-tree verification ("投机采样", section 验证方案:
  * candidate draft sequences that share a prefix are merged into a trie, and
  * the target scores every node in one pass; SpecInfer's token-tree verifier).

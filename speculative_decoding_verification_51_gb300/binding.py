@@ -49,6 +49,9 @@ def _declare(lib):
     lib.spec_verify.argtypes = common
     lib.spec_verify_ex.restype = i32
     lib.spec_verify_ex.argtypes = common + [u32, vp, vp, vp]
+    lib.spec_verify_dev_seed.restype = i32
+    lib.spec_verify_dev_seed.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp,
+                                         sz, vp, u32, vp, vp, vp]
     lib.spec_verify_tree_workspace_size.restype = sz
     lib.spec_verify_tree_workspace_size.argtypes = [i32, i32, i32]
     lib.spec_verify_tree.restype = i32
@@ -130,9 +133,13 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
                 seed: int, *, out_ids: torch.Tensor | None = None,
                 out_num_accepted: torch.Tensor | None = None,
                 workspace: torch.Tensor | None = None, stream=None, request_offset: int = 0,
-                debug: bool = False, dev_status: torch.Tensor | None = None):
+                debug: bool = False, dev_status: torch.Tensor | None = None,
+                seed_dev: torch.Tensor | None = None):
     """Verify drafts on the GPU (see include/spec_verify.h for the semantics).
 
+    seed_dev: a one-element int64 CUDA tensor; if given, the kernels read the
+    seed from it when they run (spec_verify_dev_seed, for CUDA graph capture)
+    and `seed` is ignored.
     Returns (out_ids [B, K+1] int32, out_num_accepted [B] int32), plus
     (dbg_rows [B, K+1, 4], dbg_req [B, 4]) when debug=True.
     """
@@ -167,9 +174,17 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
         dbg_req = torch.empty((B, 4), dtype=torch.float32, device=dev)
     if dev_status is not None:
         _check(dev_status, "dev_status", torch.int32, (1,), dev)
+    if seed_dev is not None:
+        _check(seed_dev, "seed_dev", torch.int64, (1,), dev)
     with torch.cuda.device(dev):
         st = _stream(stream)
-        if debug or request_offset or dev_status is not None:
+        if seed_dev is not None:
+            rc = lib().spec_verify_dev_seed(
+                _p(target_logits), dt, _p(draft_probs), _p(draft_ids), _p(num_draft),
+                _p(temperature), _p(seed_dev), B, K, V, _p(out_ids), _p(out_num_accepted),
+                _p(workspace), workspace.numel(), st, ctypes.c_uint32(request_offset & 0xFFFFFFFF),
+                _p(dbg_rows), _p(dbg_req), _p(dev_status))
+        elif debug or request_offset or dev_status is not None:
             rc = lib().spec_verify_ex(
                 _p(target_logits), dt, _p(draft_probs), _p(draft_ids), _p(num_draft),
                 _p(temperature), ctypes.c_uint64(seed & (2**64 - 1)), B, K, V, _p(out_ids),

@@ -122,7 +122,7 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
                            uint32_t request_offset, float* dbg_rows, float* dbg_req,
                            int32_t* dev_status, cudaEvent_t* events, int rule = RULE_LOSSLESS,
                            float threshold = 0.f, const int32_t* parents = nullptr,
-                           int32_t* out_last = nullptr) {
+                           int32_t* out_last = nullptr, const uint64_t* seed_dev = nullptr) {
     const bool tree = parents != nullptr;
     if (!sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
     if (rule == RULE_TYPICAL && threshold != threshold) return SPEC_ERR_INVALID_ARG;
@@ -167,6 +167,7 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     P.out_last = out_last;
     P.tmass = at<float>(workspace, L.tmass);
     P.seed = seed;
+    P.seed_dev = seed_dev;
     P.req_off = request_offset;
     P.rule = rule;
     P.threshold = threshold;
@@ -260,6 +261,21 @@ spec_status spec_verify_typical(const void* target_logits, spec_dtype logits_dty
                        seed, B, K, V, out_ids, out_num_accepted, workspace, workspace_bytes,
                        stream, request_offset, dbg_rows, dbg_req, dev_status, nullptr,
                        RULE_TYPICAL, threshold);
+}
+
+spec_status spec_verify_dev_seed(const void* target_logits, spec_dtype logits_dtype,
+                                 const float* draft_probs, const int32_t* draft_ids,
+                                 const int32_t* num_draft, const float* temperature,
+                                 const uint64_t* seed_dev, int B, int K, int V, int32_t* out_ids,
+                                 int32_t* out_num_accepted, void* workspace,
+                                 size_t workspace_bytes, spec_stream_t stream,
+                                 uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                                 int32_t* dev_status) {
+    if (!seed_dev || (reinterpret_cast<uintptr_t>(seed_dev) & 7)) return SPEC_ERR_INVALID_ARG;
+    return verify_impl(target_logits, logits_dtype, draft_probs, draft_ids, num_draft,
+                       temperature, 0, B, K, V, out_ids, out_num_accepted, workspace,
+                       workspace_bytes, stream, request_offset, dbg_rows, dbg_req, dev_status,
+                       nullptr, RULE_LOSSLESS, 0.f, nullptr, nullptr, seed_dev);
 }
 
 size_t spec_verify_tree_workspace_size(int B, int N, int V) {

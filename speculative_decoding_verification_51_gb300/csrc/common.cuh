@@ -100,6 +100,7 @@ struct Params {
     int32_t* out_last;       // [B] last accepted node
     float* tmass;            // [B, C] per-chunk masses of a tree walk's residual
     uint64_t seed;
+    const uint64_t* seed_dev;  // if set, the seed is read here when the kernels run
     uint32_t req_off;
     int rule;         // RULE_*
     float threshold;  // typical acceptance: keep x_j iff p_j(x_j) >= threshold
@@ -276,8 +277,10 @@ __device__ __forceinline__ float uniform01(uint32_t x) {
 }
 // Uniforms of row j of request b (global index b + req_off).
 __device__ __forceinline__ uint4 row_block(const Params& P, int b, int j) {
+    const uint64_t seed = P.seed_dev ? __ldg(reinterpret_cast<const unsigned long long*>(P.seed_dev))
+                                     : P.seed;
     return philox4x32_10(make_uint4(uint32_t(b) + P.req_off, uint32_t(j), 0u, 0u),
-                         uint32_t(P.seed), uint32_t(P.seed >> 32));
+                         uint32_t(seed), uint32_t(seed >> 32));
 }
 
 // ---------------------------------------------------------------- reductions

@@ -246,3 +246,41 @@ def test_lossless_chi_square_on_gpu():
         pk = np.prod(alpha[:k]) * (1 - alpha[k] if k < K else 1.0)
         f = np.mean(nacc == k)
         assert abs(f - pk) < 5 * math.sqrt(pk * (1 - pk) / B) + 1e-9
+
+
+def test_device_seed_and_graph_replay():
+    """The seed read from device memory gives the same result as the seed
+    passed by value, and a call captured in a CUDA graph replays with the
+    seed written before each replay."""
+    ensure_built()
+    w = W.make_workload(3, device="cuda")
+    B, K = w.B, w.K
+    ws = binding.new_workspace(B, K, w.V, torch.device("cuda"))
+    out = torch.empty((B, K + 1), dtype=torch.int32, device="cuda")
+    nacc = torch.empty((B,), dtype=torch.int32, device="cuda")
+    seed = torch.tensor([123456789], dtype=torch.int64, device="cuda")
+
+    def call(**kw):
+        binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
+                            w.temperature, kw.pop("s", 0), out_ids=out, out_num_accepted=nacc,
+                            workspace=ws, **kw)
+
+    call(s=123456789)
+    torch.cuda.synchronize()
+    want = (out.clone(), nacc.clone())
+    call(seed_dev=seed)
+    torch.cuda.synchronize()
+    assert torch.equal(out, want[0]) and torch.equal(nacc, want[1])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call(seed_dev=seed, stream=s)
+    for sd in (77, 123456789, 2**40 + 3):
+        seed.fill_(sd)
+        g.replay()
+        torch.cuda.synchronize()
+        got = (out.clone(), nacc.clone())
+        call(s=sd)
+        torch.cuda.synchronize()
+        assert torch.equal(got[0], out) and torch.equal(got[1], nacc), sd
