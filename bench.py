@@ -60,10 +60,12 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--mode", choices=["chain", "typical", "tree"], default="chain",
+    ap.add_argument("--mode", choices=["chain", "typical", "tree", "early_exit"], default="chain",
                     help="chain: the lossless / greedy verifier (the headline line); "
                          "typical: typical acceptance on the same workload; tree: "
-                         "token-tree verification of tries with --tree-nodes nodes")
+                         "token-tree verification of tries with --tree-nodes nodes; "
+                         "early_exit: the verifier that stops reading a request's rows at "
+                         "its first rejection, timed beside the all-rows verifier")
     ap.add_argument("--threshold", type=float, default=0.01, help="typical acceptance threshold")
     ap.add_argument("--tree-nodes", type=int, default=16)
     return ap.parse_args()
@@ -377,11 +379,138 @@ def run_variant(args, rank, world, local):
         torch.distributed.destroy_process_group()
 
 
+def run_early_exit(args, rank, world, local):
+    """The early-exit verifier (one pass per draft position, requests dropped
+    at their first rejection) against the all-rows verifier on the same
+    workload: both captured in CUDA graphs with the seed in device memory,
+    replayed alternately, L2 flushed before every replay."""
+    from speculative_decoding_verification_51_gb300 import binding
+    from speculative_decoding_verification_51_gb300 import build as _build
+    from speculative_decoding_verification_51_gb300 import workloads as W
+    from speculative_decoding_verification_51_gb300 import sharding
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+    binding.lib()
+    w = W.make_workload(args.config, device=dev)
+    if args.batch:
+        w = w.leading(args.batch)
+    B, K, V = w.B, w.K, w.V
+    esz = 2 if w.target_logits.dtype == torch.bfloat16 else 4
+    offset = sharding.weak_offset(rank, B)
+    pos = W.positions(w.num_draft)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2(i):
+        flush.fill_(i & 0xFF)
+        flush_rd.sum()
+
+    seed_buf = torch.zeros(1, dtype=torch.int64, device=dev)
+    graphs, outs, keep = {}, {}, {}
+    for name, ee in (("all_rows", False), ("early_exit", True)):
+        ws = binding.new_workspace(B, K, V, dev)
+        oi = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+        on = torch.empty((B,), dtype=torch.int32, device=dev)
+
+        def call(st, ws=ws, oi=oi, on=on, ee=ee):
+            binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
+                                w.temperature, 0, out_ids=oi, out_num_accepted=on,
+                                workspace=ws, request_offset=offset, seed_dev=seed_buf,
+                                stream=st, early_exit=ee)
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            call(cap)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            call(cap)
+        torch.cuda.synchronize()
+        # the graph keeps the raw pointers: hold its buffers for its lifetime
+        graphs[name], outs[name], keep[name] = g, (oi, on), ws
+    for i in range(args.warmup):
+        for g in graphs.values():
+            flush_l2(i)
+            seed_buf.fill_(1500 + i)
+            g.replay()
+    torch.cuda.synchronize()
+
+    evs = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)] for n in graphs}
+    nacc_log = torch.empty((args.steps, B), dtype=torch.int32, device=dev)
+    same = torch.ones(args.steps, dtype=torch.bool, device=dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        for i in range(args.steps):
+            seed_buf.fill_(2000 + i)
+            for n, g in graphs.items():
+                flush_l2(i + 7)
+                evs[n][i][0].record(stream)
+                g.replay()
+                evs[n][i][1].record(stream)
+            nacc_log[i].copy_(outs["early_exit"][1])
+            same[i] = (outs["early_exit"][0] == outs["all_rows"][0]).all() & \
+                (outs["early_exit"][1] == outs["all_rows"][1]).all()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = {n: sharding.max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e), device=dev)
+          for n, e in evs.items()}
+    nl = nacc_log.cpu().long()
+    n = w.num_draft.cpu().long()
+    valid = nl >= 0
+    rows_read = float(((nl + 1) * valid).sum(1).float().mean())
+    rows_all = float(((n + 1) * valid[0]).sum())
+    sampling = (w.temperature.cpu() > 0)
+    resid = float(((nl < n) & valid & sampling).sum(1).float().mean())
+    small = B * (K * 4 + 8) + B * ((K + 1) * 4 + 4)
+    algo_ee = rows_read * V * esz + resid * V * 4 + small
+    algo_all = rows_all * V * esz + resid * V * 4 + small
+    peak, peak_kind, _ = measured_peak()
+    gbs = algo_ee / (ms["early_exit"] * 1e-3) / 1e9
+    wname = workload_name(args.config, args.batch)
+    line = {
+        "metric": METRIC, "value": world * pos / (ms["early_exit"] * 1e-3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms["early_exit"], 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "mode": "early_exit",
+        "config": {"workload": f"{wname}: {w.spec.description}", "B": B, "K": K, "V": V,
+                   "positions_per_step": pos,
+                   "l2": "flushed before every timed replay: 256 MiB write, then 256 MiB read",
+                   "launch": "each verifier captured in its own CUDA graph (seed in device "
+                             "memory), the two replayed alternately"},
+        "all_rows_ms_per_step": round(ms["all_rows"], 5),
+        "speedup_vs_all_rows": round(ms["all_rows"] / ms["early_exit"], 4),
+        "outputs_identical_all_steps": bool(same.all().item()),
+        "rows_read_per_step": rows_read, "rows_all_rows_pass": rows_all,
+        "bytes_early_exit": algo_ee, "bytes_all_rows": algo_all,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None, "kernel": "whole call",
+                     "algorithmic_bytes_per_launch": algo_ee, "peak_kind": peak_kind},
+        "gpu_launches": (K + 4) * args.steps, "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.mode == "early_exit":
+        run_early_exit(args, rank, world, local)
         return
     if args.mode != "chain":
         run_variant(args, rank, world, local)

@@ -191,6 +191,40 @@ spec_status spec_verify_dev_seed(const void* target_logits, spec_dtype logits_dt
                                  int32_t* dev_status);
 
 /*
+ * spec_verify_early_exit -- spec_verify_ex that stops reading a request's rows
+ * at its first rejection ("RTP-LLM Speculative Engine", 拒绝采样算法: the
+ * per-draft loop breaks at the first rejected token, so no later position of
+ * that request is ever scored).
+ *
+ * The call runs K + 1 passes over the logits: pass r reads row r of exactly
+ * the requests that kept drafts 0..r-1 (all requests in pass 0), tests draft r
+ * (or, at r = num_draft[b], takes the bonus row) and drops every request that
+ * ends there.  The rows a request does read get the same arithmetic and the
+ * same Philox uniforms as in spec_verify, so every output equals spec_verify's
+ * on the same inputs, with two differences in what is checked: every draft id
+ * is range-checked before the first pass (as spec_verify does), but a
+ * sampling row that is never read is never checked for being all -inf (in
+ * spec_verify such a row anywhere in 0..num_draft[b] makes the request bad),
+ * and dbg_rows entries of rows that were not read hold NaN with accept = -1.
+ * Logit bytes read: sum over requests of (a_b + 1) * V * elem_size, against
+ * (num_draft[b] + 1) * V * elem_size for spec_verify; the price is K + 1
+ * dependent kernel launches instead of one.  seed_dev: NULL (the seed is
+ * `seed`), or an 8-byte aligned device pointer read in its place when the
+ * kernels run, as in spec_verify_dev_seed (for CUDA graph replay; misaligned
+ * is SPEC_ERR_INVALID_ARG).  Other arguments, workspace
+ * (spec_verify_workspace_size), errors and the device status word as
+ * spec_verify_ex.
+ */
+spec_status spec_verify_early_exit(const void* target_logits, spec_dtype logits_dtype,
+                                   const float* draft_probs, const int32_t* draft_ids,
+                                   const int32_t* num_draft, const float* temperature,
+                                   uint64_t seed, int B, int K, int V, int32_t* out_ids,
+                                   int32_t* out_num_accepted, void* workspace,
+                                   size_t workspace_bytes, spec_stream_t stream,
+                                   uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                                   int32_t* dev_status, const uint64_t* seed_dev);
+
+/*
  * spec_verify_tree -- token-tree verification ("投机采样", section 验证方案:
  * candidate draft sequences that share a prefix are merged into a trie, and
  * the target scores every node in one pass; SpecInfer's token-tree verifier).

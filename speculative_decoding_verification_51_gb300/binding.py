@@ -52,6 +52,8 @@ def _declare(lib):
     lib.spec_verify_dev_seed.restype = i32
     lib.spec_verify_dev_seed.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp,
                                          sz, vp, u32, vp, vp, vp]
+    lib.spec_verify_early_exit.restype = i32
+    lib.spec_verify_early_exit.argtypes = common + [u32, vp, vp, vp, vp]
     lib.spec_verify_tree_workspace_size.restype = sz
     lib.spec_verify_tree_workspace_size.argtypes = [i32, i32, i32]
     lib.spec_verify_tree.restype = i32
@@ -134,12 +136,14 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
                 out_num_accepted: torch.Tensor | None = None,
                 workspace: torch.Tensor | None = None, stream=None, request_offset: int = 0,
                 debug: bool = False, dev_status: torch.Tensor | None = None,
-                seed_dev: torch.Tensor | None = None):
+                seed_dev: torch.Tensor | None = None, early_exit: bool = False):
     """Verify drafts on the GPU (see include/spec_verify.h for the semantics).
 
     seed_dev: a one-element int64 CUDA tensor; if given, the kernels read the
     seed from it when they run (spec_verify_dev_seed, for CUDA graph capture)
     and `seed` is ignored.
+    early_exit: read each request's rows only up to its first rejection, one
+    pass per draft position (spec_verify_early_exit); same outputs.
     Returns (out_ids [B, K+1] int32, out_num_accepted [B] int32), plus
     (dbg_rows [B, K+1, 4], dbg_req [B, 4]) when debug=True.
     """
@@ -178,7 +182,14 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
         _check(seed_dev, "seed_dev", torch.int64, (1,), dev)
     with torch.cuda.device(dev):
         st = _stream(stream)
-        if seed_dev is not None:
+        if early_exit:
+            rc = lib().spec_verify_early_exit(
+                _p(target_logits), dt, _p(draft_probs), _p(draft_ids), _p(num_draft),
+                _p(temperature), ctypes.c_uint64(seed & (2**64 - 1)), B, K, V, _p(out_ids),
+                _p(out_num_accepted), _p(workspace), workspace.numel(), st,
+                ctypes.c_uint32(request_offset & 0xFFFFFFFF), _p(dbg_rows), _p(dbg_req),
+                _p(dev_status), _p(seed_dev))
+        elif seed_dev is not None:
             rc = lib().spec_verify_dev_seed(
                 _p(target_logits), dt, _p(draft_probs), _p(draft_ids), _p(num_draft),
                 _p(temperature), _p(seed_dev), B, K, V, _p(out_ids), _p(out_num_accepted),

@@ -21,6 +21,11 @@
 // Under the typical-acceptance rule ("投机采样" 验收标准, Typical Acceptance)
 // step 2 keeps x_j iff p > 0 and p >= the call's threshold (no q, no u_j) and
 // every sampling request is queued as a draw from p at row a_b.
+// Early exit (P.round = r >= 0): the pass holds row r only, and every earlier
+// draft of the request was kept.  The same steps run on that one row: a kept
+// draft is written out and row r + 1 joins the list of the next round;
+// otherwise the request ends here with a_b = r, exactly as the all-rows pass
+// would have ended it.
 // Values written by other warps during the same kernel (partials, gathered
 // logits) are read through L2 (ld.global.cg), after the caller's fence.
 #pragma once
@@ -86,14 +91,19 @@ __device__ __noinline__ void accept_request(const Params& P, int b) {
     const bool greedy = (T == 0.f);
     const float kappa = greedy ? 0.f : kappa_of(T);
 
+    // rows jlo..jhi are in this pass: all of them, or one early-exit round's
+    const bool ee = P.round >= 0;
+    const int jlo = ee ? P.round : 0, jhi = ee ? P.round : n;
+    const bool row_lane = lane >= jlo && lane <= jhi;
+
     // loads that do not depend on the merge go first
-    const bool draft_lane = lane < n;
+    const bool draft_lane = row_lane && lane < n;
     const int x = draft_lane ? P.ids[(size_t)b * P.K + lane] : -1;
     float2 g = make_float2(0.f, 0.f);
     if (draft_lane && !greedy) g = __ldcg(P.gath + (size_t)b * K1 + lane);
     const bool typical = P.rule == RULE_TYPICAL;
     uint4 rb = make_uint4(0, 0, 0, 0);
-    if (!greedy && lane <= n) rb = row_block(P, b, lane);
+    if (!greedy && row_lane) rb = row_block(P, b, lane);
 
     // 1. per-row merge, four rows at a time; lane j keeps row j.  With at most
     // 128 chunks per row a lane's chunks stay in registers: the row max first
@@ -105,14 +115,14 @@ __device__ __noinline__ void accept_request(const Params& P, int b) {
     const Partial* pb = P.part + (size_t)b * K1 * P.C;
     constexpr int NPL = 4;  // chunks per lane held in registers
     if (P.C <= 32 * NPL) {
-        for (int j0 = 0; j0 <= n; j0 += 4) {
+        for (int j0 = jlo; j0 <= jhi; j0 += 4) {
             Partial q[4][NPL];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
                 for (int i = 0; i < NPL; ++i) {
                     const int c = lane + 32 * i;
-                    if (j0 + jj <= n && c < P.C) {
+                    if (j0 + jj <= jhi && c < P.C) {
                         const double2 raw = __ldcg(reinterpret_cast<const double2*>(
                             pb + (size_t)(j0 + jj) * P.C + c));
                         q[jj][i] = *reinterpret_cast<const Partial*>(&raw);
@@ -124,7 +134,7 @@ __device__ __noinline__ void accept_request(const Params& P, int b) {
                 }
 #pragma unroll 1
             for (int jj = 0; jj < 4; ++jj) {
-                if (j0 + jj > n) break;
+                if (j0 + jj > jhi) break;
                 float lm = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < NPL; ++i) lm = fmaxf(lm, q[jj][i].m);
@@ -155,7 +165,7 @@ __device__ __noinline__ void accept_request(const Params& P, int b) {
             }
         }
     } else {  // long vocabularies: pairwise merges over the lane's chunks
-        for (int j = 0; j <= n; ++j) {
+        for (int j = jlo; j <= jhi; ++j) {
             float m = -INFINITY;
             int am = INT_MAX;
             float z = 0.f;
@@ -186,7 +196,7 @@ __device__ __noinline__ void accept_request(const Params& P, int b) {
 
     // 2. validation of the draft ids and rows this request uses
     const unsigned bad_id = __ballot_sync(0xffffffffu, draft_lane && (x < 0 || x >= P.V));
-    const unsigned empty = __ballot_sync(0xffffffffu, !greedy && lane <= n && my_m == -INFINITY);
+    const unsigned empty = __ballot_sync(0xffffffffu, !greedy && row_lane && my_m == -INFINITY);
     if (bad_id | empty) {
         fail((bad_id ? int(SPEC_BADBIT_DRAFT_ID) : 0) | (empty ? int(SPEC_BADBIT_EMPTY_ROW) : 0));
         return;
@@ -215,15 +225,38 @@ __device__ __noinline__ void accept_request(const Params& P, int b) {
         }
     }
 
+    auto write_dbg = [&]() {
+        float* d = P.dbg_rows + ((size_t)b * K1 + lane) * 4;
+        if (draft_lane) {
+            d[0] = greedy ? NaN : p;
+            d[1] = greedy ? NaN : u;
+            d[2] = greedy ? NaN : float(my_Z);
+            d[3] = acc ? 1.f : 0.f;
+        } else {
+            d[0] = d[1] = d[2] = NaN;
+            d[3] = -1.f;
+        }
+    };
+
     // 3. first rejection
     const unsigned accm = __ballot_sync(0xffffffffu, acc);
-    const int a = min(n, __ffs(~accm) - 1);
+    if (ee && ((accm >> jlo) & 1u)) {  // early exit: draft jlo kept, row jlo + 1 is next
+        if (lane == jlo) {
+            out[jlo] = x;
+            const int i = atomicAdd(&P.hdr[HDR_ROUND + jlo + 1], 1);
+            P.rowlist[(size_t)(jlo + 1) * P.B + i] = b * K1 + jlo + 1;
+            if (P.dbg_rows) write_dbg();
+        }
+        return;
+    }
+    const int a = ee ? jlo : min(n, __ffs(~accm) - 1);
 
-    // 4. outputs
-    if (lane < a)
-        out[lane] = x;
-    else if (lane > a && lane < K1)
+    // 4. outputs (early exit wrote the kept drafts round by round)
+    if (lane < a) {
+        if (!ee) out[lane] = x;
+    } else if (lane > a && lane < K1) {
         out[lane] = -1;
+    }
     if (greedy && lane == a) out[a] = my_amax;
     if (lane == 0) P.out_nacc[b] = a;
     if (!greedy && lane == a) {
@@ -246,18 +279,7 @@ __device__ __noinline__ void accept_request(const Params& P, int b) {
             P.bonus_rec[i] = r;
         }
     }
-    if (P.dbg_rows && lane < K1) {
-        float* d = P.dbg_rows + ((size_t)b * K1 + lane) * 4;
-        if (draft_lane) {
-            d[0] = greedy ? NaN : p;
-            d[1] = greedy ? NaN : u;
-            d[2] = greedy ? NaN : float(my_Z);
-            d[3] = acc ? 1.f : 0.f;
-        } else {
-            d[0] = d[1] = d[2] = NaN;
-            d[3] = -1.f;
-        }
-    }
+    if (P.dbg_rows && lane < K1 && lane >= jlo) write_dbg();
     if (P.dbg_req && greedy && lane == 0) {
         float* d = P.dbg_req + (size_t)b * 4;
         d[0] = float(MODE_GREEDY);

@@ -122,7 +122,8 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
                            uint32_t request_offset, float* dbg_rows, float* dbg_req,
                            int32_t* dev_status, cudaEvent_t* events, int rule = RULE_LOSSLESS,
                            float threshold = 0.f, const int32_t* parents = nullptr,
-                           int32_t* out_last = nullptr, const uint64_t* seed_dev = nullptr) {
+                           int32_t* out_last = nullptr, const uint64_t* seed_dev = nullptr,
+                           bool early_exit = false) {
     const bool tree = parents != nullptr;
     if (!sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
     if (rule == RULE_TYPICAL && threshold != threshold) return SPEC_ERR_INVALID_ARG;
@@ -162,6 +163,7 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     P.rsum = at<float>(workspace, L.rsum);
     P.gath = at<float2>(workspace, L.gath);
     P.cnt = at<int>(workspace, L.cnt);
+    P.round = early_exit ? 0 : -1;
     P.tree = tree ? 1 : 0;
     P.parents = parents;
     P.out_last = out_last;
@@ -194,9 +196,21 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     cudaError_t e = mark(0);
     if (e == cudaSuccess) e = launch(k_plan, 1, PLAN_THREADS, 0, st, false, P);
     if (e == cudaSuccess) e = mark(1);
-    if (e == cudaSuccess)
+    if (early_exit) {
+        // one pass per draft position: pass r reads row r of the requests that
+        // kept drafts 0..r-1; a request leaves at its first rejection
+        long long gr = (long long)dev.sms * (bf16 ? dev.stats_blocks_bf16 : dev.stats_blocks_f32);
+        const long long need = ((long long)B * P.C + STATS_WARPS - 1) / STATS_WARPS;
+        if (gr > need) gr = need;
+        for (int r = 0; r <= K && e == cudaSuccess; ++r) {
+            P.round = r;
+            e = launch(bf16 ? k_row_stats_bf16 : k_row_stats_f32, unsigned(gr), STATS_WARPS * 32,
+                       stats_smem(logits_dtype), st, true, P);
+        }
+    } else if (e == cudaSuccess) {
         e = launch(bf16 ? k_row_stats_bf16 : k_row_stats_f32, unsigned(g1),
                    STATS_WARPS * 32, stats_smem(logits_dtype), st, true, P);
+    }
     if (e == cudaSuccess) e = mark(2);
     if (tree) {  // the walks, one CTA per request
         if (e == cudaSuccess)
@@ -276,6 +290,21 @@ spec_status spec_verify_dev_seed(const void* target_logits, spec_dtype logits_dt
                        temperature, 0, B, K, V, out_ids, out_num_accepted, workspace,
                        workspace_bytes, stream, request_offset, dbg_rows, dbg_req, dev_status,
                        nullptr, RULE_LOSSLESS, 0.f, nullptr, nullptr, seed_dev);
+}
+
+spec_status spec_verify_early_exit(const void* target_logits, spec_dtype logits_dtype,
+                                   const float* draft_probs, const int32_t* draft_ids,
+                                   const int32_t* num_draft, const float* temperature,
+                                   uint64_t seed, int B, int K, int V, int32_t* out_ids,
+                                   int32_t* out_num_accepted, void* workspace,
+                                   size_t workspace_bytes, spec_stream_t stream,
+                                   uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                                   int32_t* dev_status, const uint64_t* seed_dev) {
+    if (reinterpret_cast<uintptr_t>(seed_dev) & 7) return SPEC_ERR_INVALID_ARG;
+    return verify_impl(target_logits, logits_dtype, draft_probs, draft_ids, num_draft,
+                       temperature, seed, B, K, V, out_ids, out_num_accepted, workspace,
+                       workspace_bytes, stream, request_offset, dbg_rows, dbg_req, dev_status,
+                       nullptr, RULE_LOSSLESS, 0.f, nullptr, nullptr, seed_dev, true);
 }
 
 size_t spec_verify_tree_workspace_size(int B, int N, int V) {

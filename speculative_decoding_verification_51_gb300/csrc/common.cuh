@@ -47,7 +47,9 @@ constexpr int STATS_STAGES = SV_STATS_STAGES; // bulk-copy stages per warp
 constexpr int SAMPLE_WARPS = SV_SAMPLE_WARPS;  // warps per k_sample CTA (2 staging buffers each)
 constexpr int PLAN_THREADS = 1024;
 
-enum { HDR_ROWS = 0, HDR_NRES = 1, HDR_NBONUS = 2, HDR_STATUS = 3, HDR_INTS = 64 };
+// HDR_ROUND + r: rows of early-exit round r (r >= 1), listed at rowlist + r * B
+enum { HDR_ROWS = 0, HDR_NRES = 1, HDR_NBONUS = 2, HDR_STATUS = 3, HDR_ROUND = 8, HDR_INTS = 64 };
+static_assert(HDR_ROUND + SPEC_MAX_K + 1 <= HDR_INTS, "round counters overflow the header");
 enum { MODE_BAD = -1, MODE_GREEDY = 0, MODE_RESIDUAL = 1, MODE_BONUS = 2, MODE_FALLBACK = 3,
        MODE_TYPICAL = 4 };
 // acceptance rule of a call: the lossless test u <= p / q, or typical
@@ -93,6 +95,10 @@ struct Params {
     float* rsum;      // [B*C] residual chunk sums (TILE-token chunks)
     float2* gath;     // [B*(K+1)] {l_j(x_j), q_j(x_j)} gathered by k_row_stats
     int* cnt;         // [B] (row, chunk) tiles of each request finished so far
+    // early exit (round >= 0): this pass verifies row `round` of the requests
+    // that accepted drafts 0..round-1; acceptance appends each survivor's next
+    // row to the list of round + 1.  round = -1: every row in one pass.
+    int round;
     // token-tree verification (tree != 0): row v of request b is node v, row c
     // of probs the draft distribution of node c; parents[b * K1 + c] < c
     int tree;

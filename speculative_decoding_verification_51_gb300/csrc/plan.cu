@@ -16,6 +16,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_plan(Params P) {
     __shared__ int carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     griddep_launch_dependents();
+    if (tid < SPEC_MAX_K + 1) P.hdr[HDR_ROUND + tid] = 0;
     if (tid == 0) {
         P.hdr[HDR_NRES] = 0;
         P.hdr[HDR_NBONUS] = 0;
@@ -43,7 +44,13 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_plan(Params P) {
                        P.rule == RULE_LOSSLESS) {
                 flags |= SPEC_BADBIT_NO_PROBS;
             }
-            rows = flags ? 0 : (P.tree ? n : n + 1);
+            if (!flags && P.round == 0)  // early exit: every draft id is checked up front
+                for (int j = 0; j < n; ++j) {
+                    const int x = P.ids[(size_t)b * P.K + j];
+                    if (x < 0 || x >= P.V) flags |= SPEC_BADBIT_DRAFT_ID;
+                }
+            // early exit starts with row 0 of every request
+            rows = flags ? 0 : (P.tree ? n : (P.round == 0 ? 1 : n + 1));
             P.req_flags[b] = flags;
             P.cnt[b] = 0;
             flags_any |= flags;

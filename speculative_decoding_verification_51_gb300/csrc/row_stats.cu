@@ -101,9 +101,9 @@ struct RowCtx {
     int xchunk;    // chunk holding xj (-1: none)
 };
 
-__device__ __forceinline__ RowCtx row_ctx(const Params& P, long long r) {
+__device__ __forceinline__ RowCtx row_ctx(const Params& P, const int* rowlist, long long r) {
     RowCtx rc;
-    rc.slot = P.rowlist[r];
+    rc.slot = rowlist[r];
     const int b = rc.slot / P.K1, j = rc.slot - b * P.K1;
     rc.b = b;
     rc.n = P.num_draft[b];
@@ -140,7 +140,10 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
     griddep_launch_dependents();
     griddep_wait();  // the row list of k_plan
 
-    const long long R = P.hdr[HDR_ROWS];
+    // the rows of this pass: all of them, or those of one early-exit round
+    const bool later_round = P.round > 0;
+    const int* rowlist = later_round ? P.rowlist + (size_t)P.round * P.B : P.rowlist;
+    const long long R = later_round ? __ldcg(P.hdr + HDR_ROUND + P.round) : P.hdr[HDR_ROWS];
     const long long T = R * P.C;
     const long long W = (long long)gridDim.x * STATS_WARPS;
     const long long w = (long long)blockIdx.x * STATS_WARPS + warp;
@@ -153,7 +156,7 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
     // producer (lane 0): next tile to issue, as (row, chunk), and its row's slot
     long long pr = r0;
     int pc = c0;
-    int pslot = lane == 0 ? P.rowlist[r0] : 0;
+    int pslot = lane == 0 ? rowlist[r0] : 0;
     auto issue = [&](int s) {
         const int nel = min(TILE, P.V - pc * TILE);
         const uint32_t bytes = uint32_t(nel) * TL::ESZ;
@@ -163,7 +166,7 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
         bulk_g2s(buf + s * TL::BYTES, src, bytes, &bars[warp][s]);
         if (++pc == P.C) {
             pc = 0;
-            if (++pr < R) pslot = P.rowlist[pr];
+            if (++pr < R) pslot = rowlist[pr];
         }
     };
     if (lane == 0) {
@@ -173,7 +176,7 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
     // consumer state
     long long cr = r0;
     int cc = c0;
-    RowCtx rc = row_ctx(P, cr);
+    RowCtx rc = row_ctx(P, rowlist, cr);
     float qx = 0.f;  // q_j(x_j), fetched at row start by the warp that owns x_j's tile
     auto prefetch_q = [&]() {
         const long long t_x = cr * P.C + rc.xchunk;
@@ -190,7 +193,9 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
         int last = 0;
         if (lane == 0 && seg_tiles > 0 && !P.tree) {  // trees are walked by k_tree_walk
             __threadfence();  // this warp's partials before its count
-            const int total = (seg_n + 1) * P.C;
+            // an early-exit request completes one row per round; its count
+            // is never reset, so round r ends at (r + 1) * C
+            const int total = (P.round >= 0 ? P.round + 1 : seg_n + 1) * P.C;
             last = atomicAdd(&P.cnt[seg_b], seg_tiles) + seg_tiles == total;
         }
         if (__shfl_sync(0xffffffffu, last, 0)) {
@@ -318,7 +323,7 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
         if (++cc == P.C) {
             cc = 0;
             if (++cr < R && i + 1 < n_tiles) {
-                rc = row_ctx(P, cr);
+                rc = row_ctx(P, rowlist, cr);
                 prefetch_q();
                 if (rc.b != seg_b) {  // the warp moves on to the next request
                     flush();
