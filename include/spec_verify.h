@@ -225,6 +225,26 @@ spec_status spec_verify_early_exit(const void* target_logits, spec_dtype logits_
                                    int32_t* dev_status, const uint64_t* seed_dev);
 
 /*
+ * spec_lmhead_logits -- the target's logits from its last hidden states: the
+ * vocabulary projection of the one target pass that scores the drafts
+ * ("投机采样", 第二步: one forward of the target yields p_1 .. p_{gamma+1};
+ * "深入推测解码" 保证原始分布 step 2), on the tcgen05 tensor cores.
+ *
+ *   hidden      [rows, H] bf16, row-major, 16-byte aligned (device).
+ *   lm_head     [V, H] bf16, row-major (token v's output embedding), aligned.
+ *   logits_out  [rows, V] bf16 (written): logits[r, v] = sum_h hidden[r, h] *
+ *               lm_head[v, h], products and sums in float32, rounded once to
+ *               bf16 (nearest, ties to even).
+ *   dev_status  one device int32; SPEC_BADBIT_TIMEOUT is or-ed in if a wait
+ *               of the kernel ran out (the outputs are then incomplete).
+ * H must be a multiple of 64 and V of 8 (else SPEC_ERR_UNSUPPORTED);
+ * 1 <= H <= 65536, V <= 2^24, rows <= 2^24.  Enqueues one kernel on
+ * `stream`; allocates nothing and does not synchronise.
+ */
+spec_status spec_lmhead_logits(const void* hidden, const void* lm_head, int rows, int H, int V,
+                               void* logits_out, int32_t* dev_status, spec_stream_t stream);
+
+/*
  * spec_verify_tree -- token-tree verification ("投机采样", section 验证方案:
  * candidate draft sequences that share a prefix are merged into a trie, and
  * the target scores every node in one pass; SpecInfer's token-tree verifier).

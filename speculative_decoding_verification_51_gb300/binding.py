@@ -54,6 +54,8 @@ def _declare(lib):
                                          sz, vp, u32, vp, vp, vp]
     lib.spec_verify_early_exit.restype = i32
     lib.spec_verify_early_exit.argtypes = common + [u32, vp, vp, vp, vp]
+    lib.spec_lmhead_logits.restype = i32
+    lib.spec_lmhead_logits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     lib.spec_verify_tree_workspace_size.restype = sz
     lib.spec_verify_tree_workspace_size.argtypes = [i32, i32, i32]
     lib.spec_verify_tree.restype = i32
@@ -381,4 +383,29 @@ def philox_fill(seed: int, ctrs: torch.Tensor, stream=None) -> torch.Tensor:
                                     ctrs.numel() // 4, _p(out), _stream(stream))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_philox_fill")
+    return out
+
+
+def lmhead_logits(hidden: torch.Tensor, lm_head: torch.Tensor, *, out: torch.Tensor | None = None,
+                  dev_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """bf16 logits = hidden [rows, H] @ lm_head [V, H]^T on the tensor cores
+    (include/spec_verify.h, spec_lmhead_logits)."""
+    if hidden.dim() != 2 or lm_head.dim() != 2 or hidden.shape[1] != lm_head.shape[1]:
+        raise ValueError("hidden must be [rows, H] and lm_head [V, H]")
+    rows, H = hidden.shape
+    V = lm_head.shape[0]
+    dev = hidden.device
+    _check(hidden, "hidden", torch.bfloat16, device=dev)
+    _check(lm_head, "lm_head", torch.bfloat16, device=dev)
+    if out is None:
+        out = torch.empty((rows, V), dtype=torch.bfloat16, device=dev)
+    _check(out, "out", torch.bfloat16, (rows, V), dev)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(dev_status, "dev_status", torch.int32, (1,), dev)
+    with torch.cuda.device(dev):
+        rc = lib().spec_lmhead_logits(_p(hidden), _p(lm_head), rows, H, V, _p(out), _p(dev_status),
+                                      _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_lmhead_logits")
     return out
