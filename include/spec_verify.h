@@ -245,6 +245,36 @@ spec_status spec_lmhead_logits(const void* hidden, const void* lm_head, int rows
                                void* logits_out, int32_t* dev_status, spec_stream_t stream);
 
 /*
+ * spec_verify_lmhead -- spec_verify_ex with the target logits produced inside
+ * the call from the target's last hidden states (the fused logits producer):
+ * the rows the verifier reads (j <= num_draft[b]) are projected by the
+ * tcgen05 LM-head GEMM of spec_lmhead_logits, and the same kernel's epilogue
+ * takes, from the bf16 logits it stores, the row statistics and the
+ * acceptance that spec_verify's row pass would take.  The logits make one
+ * trip to HBM (written) instead of two (written by a separate GEMM, then
+ * read back).
+ *
+ *   hidden      [B, K+1, H] bf16 (row j of request b: the hidden state whose
+ *               projection is target_logits[b, j] of spec_verify).
+ *   lm_head     [V, H] bf16.
+ *   logits_out  [B, K+1, V] bf16 (written for the rows read, left as it was
+ *               elsewhere); the residual and bonus draws read it afterwards.
+ *   workspace   at least spec_verify_lmhead_workspace_size(B, K, V, H) bytes.
+ * Other arguments, outputs and errors as spec_verify_ex with bf16 logits;
+ * H must be a multiple of 64 (else SPEC_ERR_UNSUPPORTED).  The outputs equal
+ * spec_verify's on logits_out up to the float32 summation order of the row
+ * statistics.
+ */
+size_t spec_verify_lmhead_workspace_size(int B, int K, int V, int H);
+spec_status spec_verify_lmhead(const void* hidden, const void* lm_head, int H, void* logits_out,
+                               const float* draft_probs, const int32_t* draft_ids,
+                               const int32_t* num_draft, const float* temperature, uint64_t seed,
+                               int B, int K, int V, int32_t* out_ids, int32_t* out_num_accepted,
+                               void* workspace, size_t workspace_bytes, spec_stream_t stream,
+                               uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                               int32_t* dev_status);
+
+/*
  * spec_verify_tree -- token-tree verification ("投机采样", section 验证方案:
  * candidate draft sequences that share a prefix are merged into a trie, and
  * the target scores every node in one pass; SpecInfer's token-tree verifier).

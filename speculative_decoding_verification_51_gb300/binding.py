@@ -54,6 +54,11 @@ def _declare(lib):
                                          sz, vp, u32, vp, vp, vp]
     lib.spec_verify_early_exit.restype = i32
     lib.spec_verify_early_exit.argtypes = common + [u32, vp, vp, vp, vp]
+    lib.spec_verify_lmhead_workspace_size.restype = sz
+    lib.spec_verify_lmhead_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.spec_verify_lmhead.restype = i32
+    lib.spec_verify_lmhead.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, u64, i32, i32, i32, vp, vp,
+                                       vp, sz, vp, u32, vp, vp, vp]
     lib.spec_lmhead_logits.restype = i32
     lib.spec_lmhead_logits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     lib.spec_verify_tree_workspace_size.restype = sz
@@ -409,3 +414,62 @@ def lmhead_logits(hidden: torch.Tensor, lm_head: torch.Tensor, *, out: torch.Ten
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_lmhead_logits")
     return out
+
+
+def spec_verify_lmhead(hidden: torch.Tensor, lm_head: torch.Tensor, draft_probs: torch.Tensor | None,
+                       draft_ids: torch.Tensor, num_draft: torch.Tensor, temperature: torch.Tensor,
+                       seed: int, *, logits_out: torch.Tensor | None = None,
+                       out_ids: torch.Tensor | None = None,
+                       out_num_accepted: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None, stream=None, request_offset: int = 0,
+                       debug: bool = False, dev_status: torch.Tensor | None = None):
+    """Verification with the logits produced in the call from hidden states
+    (include/spec_verify.h, spec_verify_lmhead).
+
+    hidden [B, K+1, H] bf16, lm_head [V, H] bf16.  Returns (out_ids,
+    out_num_accepted, logits_out) plus (dbg_rows, dbg_req) when debug=True.
+    """
+    if hidden.dim() != 3 or lm_head.dim() != 2 or hidden.shape[2] != lm_head.shape[1]:
+        raise ValueError("hidden must be [B, K+1, H] and lm_head [V, H]")
+    B, K1, H = hidden.shape
+    K, V = K1 - 1, lm_head.shape[0]
+    dev = hidden.device
+    _check(hidden, "hidden", torch.bfloat16, device=dev)
+    _check(lm_head, "lm_head", torch.bfloat16, device=dev)
+    if draft_probs is not None:
+        _check(draft_probs, "draft_probs", torch.float32, (B, K, V), dev)
+    _check(draft_ids, "draft_ids", torch.int32, (B, K), dev)
+    _check(num_draft, "num_draft", torch.int32, (B,), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    if logits_out is None:
+        logits_out = torch.empty((B, K1, V), dtype=torch.bfloat16, device=dev)
+    _check(logits_out, "logits_out", torch.bfloat16, (B, K1, V), dev)
+    if out_ids is None:
+        out_ids = torch.empty((B, K1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _check(out_ids, "out_ids", torch.int32, (B, K1), dev)
+    _check(out_num_accepted, "out_num_accepted", torch.int32, (B,), dev)
+    if workspace is None:
+        n = int(lib().spec_verify_lmhead_workspace_size(B, K, V, H))
+        if n == 0:
+            raise ValueError(f"unsupported sizes B={B} K={K} V={V} H={H}")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    dbg_rows = dbg_req = None
+    if debug:
+        dbg_rows = torch.empty((B, K1, 4), dtype=torch.float32, device=dev)
+        dbg_req = torch.empty((B, 4), dtype=torch.float32, device=dev)
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, (1,), dev)
+    with torch.cuda.device(dev):
+        rc = lib().spec_verify_lmhead(
+            _p(hidden), _p(lm_head), H, _p(logits_out), _p(draft_probs), _p(draft_ids),
+            _p(num_draft), _p(temperature), ctypes.c_uint64(seed & (2**64 - 1)), B, K, V,
+            _p(out_ids), _p(out_num_accepted), _p(workspace), workspace.numel(), _stream(stream),
+            ctypes.c_uint32(request_offset & 0xFFFFFFFF), _p(dbg_rows), _p(dbg_req),
+            _p(dev_status))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify_lmhead")
+    if debug:
+        return out_ids, out_num_accepted, logits_out, dbg_rows, dbg_req
+    return out_ids, out_num_accepted, logits_out

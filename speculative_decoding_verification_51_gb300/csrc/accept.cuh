@@ -62,7 +62,7 @@ __device__ __forceinline__ void merge_argmax(float& m, int& a, float m2, int a2)
 }  // namespace
 
 // Request b (valid: k_plan has checked num_draft and temperature); whole warp.
-__device__ __noinline__ void accept_request(const Params& P, int b) {
+static __device__ __noinline__ void accept_request(const Params& P, int b) {
     const int lane = threadIdx.x & 31;
     const int K1 = P.K1;
     int32_t* out = P.out_ids + (size_t)b * K1;

@@ -123,7 +123,7 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
                            int32_t* dev_status, cudaEvent_t* events, int rule = RULE_LOSSLESS,
                            float threshold = 0.f, const int32_t* parents = nullptr,
                            int32_t* out_last = nullptr, const uint64_t* seed_dev = nullptr,
-                           bool early_exit = false) {
+                           bool early_exit = false, const LmHeadIn* lm = nullptr) {
     const bool tree = parents != nullptr;
     if (!sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
     if (rule == RULE_TYPICAL && threshold != threshold) return SPEC_ERR_INVALID_ARG;
@@ -196,7 +196,10 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     cudaError_t e = mark(0);
     if (e == cudaSuccess) e = launch(k_plan, 1, PLAN_THREADS, 0, st, false, P);
     if (e == cudaSuccess) e = mark(1);
-    if (early_exit) {
+    if (lm) {
+        // the logits are produced here, with their row statistics and acceptances
+        if (e == cudaSuccess && launch_lmhead_fused(P, *lm, st) != SPEC_OK) return SPEC_ERR_CUDA;
+    } else if (early_exit) {
         // one pass per draft position: pass r reads row r of the requests that
         // kept drafts 0..r-1; a request leaves at its first rejection
         long long gr = (long long)dev.sms * (bf16 ? dev.stats_blocks_bf16 : dev.stats_blocks_f32);
@@ -305,6 +308,37 @@ spec_status spec_verify_early_exit(const void* target_logits, spec_dtype logits_
                        temperature, seed, B, K, V, out_ids, out_num_accepted, workspace,
                        workspace_bytes, stream, request_offset, dbg_rows, dbg_req, dev_status,
                        nullptr, RULE_LOSSLESS, 0.f, nullptr, nullptr, seed_dev, true);
+}
+
+size_t spec_verify_lmhead_workspace_size(int B, int K, int V, int H) {
+    if (!sizes_ok(B, K, V) || V % 8 != 0 || H <= 0 || H % 64 != 0 || H > (1 << 16)) return 0;
+    return make_layout(B, K, V).total + align256(size_t(B) * (K + 1) * H * 2);
+}
+
+spec_status spec_verify_lmhead(const void* hidden, const void* lm_head, int H, void* logits_out,
+                               const float* draft_probs, const int32_t* draft_ids,
+                               const int32_t* num_draft, const float* temperature, uint64_t seed,
+                               int B, int K, int V, int32_t* out_ids, int32_t* out_num_accepted,
+                               void* workspace, size_t workspace_bytes, spec_stream_t stream,
+                               uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                               int32_t* dev_status) {
+    if (!sizes_ok(B, K, V) || H <= 0 || H > (1 << 16)) return SPEC_ERR_INVALID_ARG;
+    if (H % 64 != 0 || V % 8 != 0) return SPEC_ERR_UNSUPPORTED;
+    if (B == 0) return SPEC_OK;
+    if (!hidden || !lm_head || !logits_out) return SPEC_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(hidden) & 15) || (reinterpret_cast<uintptr_t>(lm_head) & 15))
+        return SPEC_ERR_UNSUPPORTED;
+    const size_t base = make_layout(B, K, V).total;
+    if (workspace_bytes < spec_verify_lmhead_workspace_size(B, K, V, H)) return SPEC_ERR_WORKSPACE;
+    LmHeadIn in;
+    in.hidden = hidden;
+    in.lm_head = lm_head;
+    in.H = H;
+    in.hid_c = static_cast<char*>(workspace) + base;
+    return verify_impl(logits_out, SPEC_BF16, draft_probs, draft_ids, num_draft, temperature, seed,
+                       B, K, V, out_ids, out_num_accepted, workspace, workspace_bytes, stream,
+                       request_offset, dbg_rows, dbg_req, dev_status, nullptr, RULE_LOSSLESS, 0.f,
+                       nullptr, nullptr, nullptr, false, &in);
 }
 
 size_t spec_verify_tree_workspace_size(int B, int N, int V) {

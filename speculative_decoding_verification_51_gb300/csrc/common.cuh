@@ -346,4 +346,16 @@ constexpr int TREE_MAX_NODES = 32;
 
 __global__ void k_philox_fill(uint64_t seed, const uint32_t* ctrs, int64_t n, uint32_t* out);
 
+// Logits produced on the tensor cores from the target's hidden states
+// (lmhead.cu): the rows k_plan listed are gathered into hid_c [rows, H], then
+// one tcgen05 GEMM writes their bf16 logits and, in its epilogue, the
+// row-statistics partials, the draft gathers and the acceptances.
+struct LmHeadIn {
+    const void* hidden;   // [B*(K+1), H] bf16
+    const void* lm_head;  // [V, H] bf16
+    int H;
+    void* hid_c;          // workspace: [B*(K+1), H] bf16, the listed rows in list order
+};
+spec_status launch_lmhead_fused(const Params& P, const LmHeadIn& in, cudaStream_t st);
+
 }  // namespace sv

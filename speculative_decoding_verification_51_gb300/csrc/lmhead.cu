@@ -16,6 +16,18 @@
 // A CTA computes a 128-row x 2048-column block: 8 sub-tiles of 256 columns,
 // one TMA box of A (128 x 64) and B (256 x 64) per K step of 64.
 //
+// The fused form (spec_verify_lmhead) reads the rows k_plan listed, writes
+// each row's logits at its slot, and in the same epilogue takes the
+// statistics k_row_stats would take from those logits: per (row, 2048-token
+// chunk) the maximum and, for sampling rows, the sum of 2^(l*kappa - c)
+// against c = RN(chunk max * kappa) (kept online over the chunk's 32-column
+// pieces, rescaled when the maximum grows), or for greedy rows the lowest
+// index of the maximum; l(x_j) and q(x_j) for the draft token; then the
+// per-request tile count and, by the warp that completes a request, its
+// acceptance (accept_request).  All of it is computed from the bf16-rounded
+// logits that are stored, so the later residual and bonus draws see the
+// same values.
+//
 // Every wait is bounded: a CTA that times out sets SPEC_BADBIT_TIMEOUT, lets
 // its copies and MMAs in flight finish (again bounded), frees its TMEM and
 // returns.
@@ -26,6 +38,7 @@
 #include <climits>
 #include <mutex>
 
+#include "accept.cuh"
 #include "common.cuh"
 
 namespace sv {
@@ -127,9 +140,10 @@ struct LmArgs {
 
 }  // namespace
 
+template <bool FUSED>
 __global__ void __launch_bounds__(LM_THREADS, 1)
     k_lmhead(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-             LmArgs L) {
+             LmArgs L, Params P) {
     extern __shared__ uint8_t lm_smem_raw[];
     __shared__ __align__(8) uint64_t full[LM_STAGES], empty[LM_STAGES], accf[2], acce[2], fin;
     __shared__ uint32_t tmem_base;
@@ -138,7 +152,8 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunk = blockIdx.x, mt = blockIdx.y;
     const int row0 = mt * LM_BM;
-    if (row0 >= L.rows) return;  // whole CTA, before any barrier or TMEM
+    const int rows = FUSED ? P.hdr[HDR_ROWS] : L.rows;  // fused: the rows k_plan listed
+    if (row0 >= rows) return;  // whole CTA, before any barrier or TMEM
     const int col0 = chunk * TILE;
     const int ncols = min(TILE, L.V - col0);
     const int nsub = (ncols + LM_BN - 1) / LM_BN;
@@ -246,37 +261,137 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
         // ---- epilogue: TMEM -> registers -> bf16 logits, one row per thread
         const int q = warp & 3;  // the TMEM lane quarter this warp may read
         const int r = row0 + q * 32 + lane;
-        for (int n = 0; n < nsub; ++n) {
-            const int acc = n & 1;
-            if (!mbar_wait_bounded(&accf[acc], uint32_t(n >> 1) & 1u, LM_WAIT_NS) || *abort_v) {
+        const bool valid = r < rows;
+        // fused: this row's slot, request and draft token
+        int slot = r, b = -1, n = 0, j = 0, x = -1;
+        bool greedy = true;
+        float kappa = 0.f, qx = 0.f;
+        if (FUSED && valid) {
+            slot = P.rowlist[r];
+            b = slot / P.K1;
+            j = slot - b * P.K1;
+            n = P.num_draft[b];
+            const float T = P.temp[b];
+            greedy = (T == 0.f);
+            kappa = greedy ? 0.f : kappa_of(T);
+            if (!greedy && j < n) {
+                const int xx = P.ids[(size_t)b * P.K + j];
+                if (xx >= 0 && xx < P.V && xx / TILE == chunk) x = xx;  // only this chunk's
+            }
+            if (x >= 0 && P.rule == RULE_LOSSLESS)
+                qx = __ldg(P.probs + ((size_t)b * P.K + j) * P.V + x);
+        }
+        float m_run = -INFINITY, z_run = 0.f, c_run = -INFINITY, lx = 0.f;
+        int amax = INT_MAX;
+        bool ok = true;
+        for (int nn = 0; nn < nsub; ++nn) {
+            const int acc = nn & 1;
+            const bool got = mbar_wait_bounded(&accf[acc], uint32_t(nn >> 1) & 1u, LM_WAIT_NS);
+            if (__any_sync(0xffffffffu, !got || *abort_v)) {
                 *abort_v = 1;
+                ok = false;
                 break;
             }
             tc_fence_after();
-            const int cbase = col0 + n * LM_BN;
+            const int cbase = col0 + nn * LM_BN;
 #pragma unroll 1
             for (int p = 0; p < LM_BN / 32; ++p) {
                 uint32_t v[32];
                 tc_ld32(tbase + (uint32_t(q * 32) << 16) + uint32_t(acc * LM_BN + p * 32), v);
                 const int c = cbase + p * 32;
-                if (r < L.rows && c < L.V) {
-                    uint4* dst = reinterpret_cast<uint4*>(L.out + (size_t)r * L.V + c);
+                if (!valid || c >= L.V) continue;
+                uint32_t w[16];
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        if (c + g * 8 < L.V) {  // V is a multiple of 8
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(v[g * 8 + 0]), __uint_as_float(v[g * 8 + 1]));
-                            w.y = pack_bf16x2(__uint_as_float(v[g * 8 + 2]), __uint_as_float(v[g * 8 + 3]));
-                            w.z = pack_bf16x2(__uint_as_float(v[g * 8 + 4]), __uint_as_float(v[g * 8 + 5]));
-                            w.w = pack_bf16x2(__uint_as_float(v[g * 8 + 6]), __uint_as_float(v[g * 8 + 7]));
-                            dst[g] = w;
+                for (int k = 0; k < 16; ++k)
+                    w[k] = pack_bf16x2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+                uint4* dst = reinterpret_cast<uint4*>(L.out + (size_t)slot * L.V + c);
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    if (c + g * 8 < L.V)  // V is a multiple of 8
+                        dst[g] = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+                if constexpr (FUSED) {
+                    // statistics of the stored (bf16) values of this piece
+                    float f[32];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        f[2 * k] = bf16_lo(w[k]);
+                        f[2 * k + 1] = bf16_hi(w[k]);
+                    }
+                    const int lim = min(32, L.V - c);
+                    float pm = -INFINITY;
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        if (k < lim) pm = fmaxf(pm, f[k]);
+                    if (greedy) {
+                        if (pm > m_run) {  // the first index of the new maximum
+                            int kf = 31;
+#pragma unroll
+                            for (int k = 31; k >= 0; --k)
+                                if (k < lim && f[k] == pm) kf = k;
+                            m_run = pm;
+                            amax = c + kf;
                         }
+                    } else {
+                        if (pm > m_run) {  // rebase the running sum onto the new offset
+                            if (z_run != 0.f)
+                                z_run = __fmul_rn(z_run, ex2_approx(rebase_arg(m_run, pm, kappa)));
+                            m_run = pm;
+                            c_run = offset_of(pm, kappa);
+                        }
+                        float zs = 0.f;
+                        if (isfinite(c_run)) {
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                if (k < lim) zs = __fadd_rn(zs, ex2_approx(fmaf(f[k], kappa, -c_run)));
+                        } else {  // offset overflows (absurdly small T): (l - max) * kappa
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                if (k < lim)
+                                    zs = __fadd_rn(zs, ex2_approx(__fmul_rn(__fsub_rn(f[k], m_run), kappa)));
+                        }
+                        z_run = __fadd_rn(z_run, zs);
+                    }
+                    if (x >= c && x < c + 32) {
+                        const int e = x - c;
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            if (k == e) lx = f[k];
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acce[acc]);
+        }
+        if constexpr (FUSED) {
+            if (ok) {
+                if (valid) {
+                    Partial o;
+                    o.m = m_run;
+                    o.amax = greedy ? amax : -1;
+                    o.z = greedy ? 0.0 : double(z_run);
+                    P.part[(size_t)slot * P.C + chunk] = o;
+                    if (x >= 0) P.gath[slot] = make_float2(lx, qx);
+                }
+                __threadfence();  // this thread's partial before the counts
+                __syncwarp();
+                // one count per request among this warp's rows; the warp whose
+                // count completes (n_b + 1) * C runs the request's acceptance
+                const unsigned same = __match_any_sync(0xffffffffu, valid ? b : -1);
+                int done_b = 0;
+                if (valid && __ffs(same) - 1 == lane) {
+                    const int cnt = __popc(same);
+                    done_b = atomicAdd(&P.cnt[b], cnt) + cnt == (n + 1) * P.C;
+                }
+                unsigned todo = __ballot_sync(0xffffffffu, done_b);
+                while (todo) {
+                    const int l = __ffs(todo) - 1;
+                    todo &= todo - 1;
+                    const int bb = __shfl_sync(0xffffffffu, b, l);
+                    __threadfence();  // every other warp's partials after the count
+                    accept_request(P, bb);
+                }
+            }
         }
     }
 
@@ -288,6 +403,20 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                      "r"(LM_TMEM_COLS)
                      : "memory");
     if (threadIdx.x == 0 && *abort_v) atomicOr(L.status, int(SPEC_BADBIT_TIMEOUT));
+}
+
+// The listed rows' hidden states, in list order (one warp per row, 16-byte
+// copies); rows past the list are left as they are.
+__global__ void __launch_bounds__(256) k_gather_rows(Params P, LmHeadIn in) {
+    const int lane = threadIdx.x & 31;
+    const int R = P.hdr[HDR_ROWS];
+    const int nvec = in.H / 8;
+    for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < R; r += gridDim.x * 8) {
+        const int slot = P.rowlist[r];
+        const uint4* src = reinterpret_cast<const uint4*>(in.hidden) + (size_t)slot * nvec;
+        uint4* dst = reinterpret_cast<uint4*>(in.hid_c) + (size_t)r * nvec;
+        for (int i = lane; i < nvec; i += 32) dst[i] = __ldg(src + i);
+    }
 }
 
 }  // namespace sv
@@ -329,7 +458,51 @@ spec_status make_map(CUtensorMap* map, const void* base, int rows, int H, int bo
     return r == CUDA_SUCCESS ? SPEC_OK : SPEC_ERR_INVALID_ARG;
 }
 
+// Per-device kernel attributes (shared memory above 48 KB), set once.
+spec_status lm_prepare() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPEC_ERR_CUDA;
+    static bool done[64] = {};
+    std::lock_guard<std::mutex> lk(g_lm_mu);
+    if (!done[dev]) {
+        if (cudaFuncSetAttribute(k_lmhead<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(LM_SMEM)) != cudaSuccess ||
+            cudaFuncSetAttribute(k_lmhead<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(LM_SMEM)) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+        done[dev] = true;
+    }
+    return SPEC_OK;
+}
+
 }  // namespace
+
+namespace sv {
+
+// Gather the listed rows' hidden states, then the fused projection + row
+// statistics + acceptance over them (after k_plan, before k_sample).
+spec_status launch_lmhead_fused(const Params& P, const LmHeadIn& in, cudaStream_t st) {
+    const int maxrows = P.B * P.K1;
+    CUtensorMap ma, mb;
+    spec_status r = make_map(&ma, in.hid_c, maxrows, in.H, LM_BM);
+    if (r != SPEC_OK) return r;
+    r = make_map(&mb, in.lm_head, P.V, in.H, LM_BN);
+    if (r != SPEC_OK) return r;
+    if (lm_prepare() != SPEC_OK) return SPEC_ERR_CUDA;
+    const int gblocks = min((maxrows + 7) / 8, 4096);
+    k_gather_rows<<<gblocks, 256, 0, st>>>(P, in);
+    LmArgs L;
+    L.rows = maxrows;
+    L.H = in.H;
+    L.V = P.V;
+    L.out = static_cast<uint16_t*>(const_cast<void*>(P.logits));
+    L.status = P.status;
+    const dim3 grid(unsigned(P.C), unsigned((maxrows + LM_BM - 1) / LM_BM));
+    k_lmhead<true><<<grid, LM_THREADS, LM_SMEM, st>>>(ma, mb, L, P);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // namespace sv
 
 extern "C" {
 
@@ -348,26 +521,17 @@ spec_status spec_lmhead_logits(const void* hidden, const void* lm_head, int rows
     if (st != SPEC_OK) return st;
     st = make_map(&mb, lm_head, V, H, LM_BN);
     if (st != SPEC_OK) return st;
-    static bool attr_done[64] = {};
-    {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPEC_ERR_CUDA;
-        std::lock_guard<std::mutex> lk(g_lm_mu);
-        if (!attr_done[dev]) {
-            if (cudaFuncSetAttribute(k_lmhead, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     int(LM_SMEM)) != cudaSuccess)
-                return SPEC_ERR_CUDA;
-            attr_done[dev] = true;
-        }
-    }
+    if (lm_prepare() != SPEC_OK) return SPEC_ERR_CUDA;
     LmArgs L;
     L.rows = rows;
     L.H = H;
     L.V = V;
     L.out = static_cast<uint16_t*>(logits_out);
     L.status = dev_status;
+    Params P = {};
     const dim3 grid(unsigned((V + TILE - 1) / TILE), unsigned((rows + LM_BM - 1) / LM_BM));
-    k_lmhead<<<grid, LM_THREADS, LM_SMEM, reinterpret_cast<cudaStream_t>(stream)>>>(ma, mb, L);
+    k_lmhead<false><<<grid, LM_THREADS, LM_SMEM, reinterpret_cast<cudaStream_t>(stream)>>>(ma, mb,
+                                                                                           L, P);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -274,3 +274,82 @@ def make_tree_workload(B, N, V, *, bf16=True, seed=0, greedy_frac=0.3, width=0.6
     return TreeWorkload(lt.to(device).contiguous(), q.to(device).contiguous(),
                         tok.to(device).contiguous(), torch.from_numpy(par).to(device).contiguous(),
                         nodes.to(device), T.to(device), seed * 7919 + 13)
+
+
+# ---------------------------------------------------------------- hidden states
+# Workloads of the fused logits producer: the target's last hidden states and
+# an LM-head matrix instead of logits.  Both operands hold small integers
+# (hidden in -3..3, LM head in -15..15 times a power of two s), so every
+# float32 partial sum of the projection is a multiple of s below 2^24 s and
+# exact in any order: the logits are the same on every path that sums in
+# float32 or wider, before the one rounding to bf16.  s = 2^round(log2(2.5 /
+# sqrt(320 H))) gives logits of standard deviation about 2.5.
+
+@dataclass
+class LmHeadWorkload:
+    hidden: torch.Tensor       # [B, K+1, H] bf16
+    lm_head: torch.Tensor      # [V, H] bf16
+    draft_probs: torch.Tensor  # [B, K, V] f32
+    draft_ids: torch.Tensor    # [B, K] int32 (-1 past num_draft)
+    num_draft: torch.Tensor    # [B] int32
+    temperature: torch.Tensor  # [B] f32 (0 = greedy)
+    seed: int
+
+    @property
+    def shape(self):
+        B, K1, H = self.hidden.shape
+        return B, K1 - 1, self.lm_head.shape[0], H
+
+
+def lmhead_scale(H: int) -> float:
+    return 2.0 ** round(float(np.log2(2.5 / np.sqrt(320.0 * H))))
+
+
+def make_lmhead_workload(B, K, V, H, *, seed=0, greedy_frac=0.25, ragged=True, noise=1.0,
+                         device="cuda") -> LmHeadWorkload:
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    K1 = K + 1
+    s = lmhead_scale(H)
+    hidden = torch.randint(-3, 4, (B, K1, H), generator=g, dtype=torch.int8)
+    hidden = hidden.to(device).to(torch.bfloat16).contiguous()
+    w = torch.randint(-15, 16, (V, H), generator=g, dtype=torch.int8)
+    lm_head = (w.to(device).to(torch.float32) * s).to(torch.bfloat16).contiguous()
+    num_draft = (torch.randint(0, K + 1, (B,), generator=g) if ragged
+                 else torch.full((B,), K)).to(torch.int32)
+    temp = 0.5 + 0.7 * torch.rand(B, generator=g)
+    temp = torch.where(torch.rand(B, generator=g) < greedy_frac, torch.zeros_like(temp), temp)
+    # the drafter sees the target's logits (exact float32 sums, bf16-rounded)
+    # plus noise; logits are formed a few rows at a time to bound memory
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    probs = torch.empty((B, K, V), dtype=torch.float32, device=device)
+    ids = torch.full((B, K), -1, dtype=torch.int32)
+    gd = torch.Generator(device=device).manual_seed(seed + 1)
+    wf = lm_head.float()
+    for b0 in range(0, B, 16):
+        b1 = min(B, b0 + 16)
+        lg = (hidden[b0:b1, :K].float() @ wf.T).to(torch.bfloat16).float()  # [bb, K, V]
+        dl = lg + noise * torch.randn(lg.shape, generator=gd, device=device)
+        t = temp[b0:b1].to(device)
+        tq = torch.where(t > 0, t, torch.ones_like(t))[:, None, None]
+        q = torch.softmax(dl / tq, dim=-1)
+        probs[b0:b1] = q
+        samp = torch.multinomial(q.reshape(-1, V), 1, generator=gd).reshape(b1 - b0, K)
+        greedy_ids = dl.argmax(-1)
+        pick = torch.where((t > 0)[:, None], samp, greedy_ids).to(torch.int32).cpu()
+        ids[b0:b1] = pick
+    torch.backends.cuda.matmul.allow_tf32 = prev
+    pos = torch.arange(K)[None, :]
+    ids = torch.where(pos < num_draft[:, None].long(), ids, torch.full_like(ids, -1))
+    return LmHeadWorkload(hidden, lm_head, probs.contiguous(), ids.to(device).contiguous(),
+                          num_draft.to(device), temp.to(torch.float32).to(device), seed * 31 + 5)
+
+
+def lmhead_to_numpy(w: LmHeadWorkload) -> dict:
+    """Host copies: operands as bf16 bit patterns, the rest as the oracle takes them."""
+    def bits(t):
+        return t.detach().cpu().view(torch.int16).numpy().view("uint16")
+    return {"hidden": bits(w.hidden), "lm_head": bits(w.lm_head),
+            "draft_probs": w.draft_probs.cpu().numpy(), "draft_ids": w.draft_ids.cpu().numpy(),
+            "num_draft": w.num_draft.cpu().numpy(), "temperature": w.temperature.cpu().numpy(),
+            "seed": w.seed}

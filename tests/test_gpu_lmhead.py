@@ -90,3 +90,55 @@ def test_lmhead_matches_torch(rows, H, V):
     exact = LM.lmhead_logits_f64(hb, wb)
     abs_sum = np.abs(LM.bf16_bits_to_f64(hb)) @ np.abs(LM.bf16_bits_to_f64(wb)).T
     assert _within_bound(_bits(out[rs, vs]), exact, abs_sum, H).all()
+
+
+# ------------------------------------------------ the fused verifier (spec_verify_lmhead)
+
+import parity  # noqa: E402
+import oracle  # noqa: E402
+from speculative_decoding_verification_51_gb300 import workloads as W  # noqa: E402
+
+
+def _fused_check(B, K, V, H, seed, **kw):
+    ensure_built()
+    w = W.make_lmhead_workload(B, K, V, H, seed=seed, **kw)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ids, nacc, logits, rows, req = binding.spec_verify_lmhead(
+        w.hidden, w.lm_head, w.draft_probs, w.draft_ids, w.num_draft, w.temperature, w.seed,
+        debug=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ids, nacc, rows = ids.cpu().numpy(), nacc.cpu().numpy(), rows.cpu().numpy()
+    inp = W.lmhead_to_numpy(w)
+    # the oracle's own logits: exact sums (integer operands), one bf16 rounding
+    lo = LM.lmhead_logits(inp["hidden"].reshape(-1, H), inp["lm_head"]).reshape(B, K + 1, V)
+    n = inp["num_draft"]
+    got = _bits(logits)
+    for b in range(B):  # the rows the verifier reads are written, bit for bit
+        assert np.array_equal(got[b, : n[b] + 1], lo[b, : n[b] + 1]), b
+    vin = {"target_logits": lo, "draft_probs": inp["draft_probs"], "draft_ids": inp["draft_ids"],
+           "num_draft": n, "temperature": inp["temperature"], "seed": inp["seed"]}
+    ref = oracle.spec_verify(**vin)
+    rep = parity.compare(vin, ids, nacc, rows, ref)
+    print(f"[lmhead B{B} K{K} V{V} H{H}] {rep.summary()}")
+    assert not rep.failures, rep.failures[:5]
+    assert rep.max_p_rel <= 1e-5
+    assert rep.excused <= max(1, 0.01 * rep.sampling), rep.summary()
+    return rep
+
+
+@pytest.mark.parametrize("B,K,V,H,greedy", [(40, 4, 4104, 128, 0.25), (24, 3, 2056, 64, 1.0),
+                                            (33, 5, 8200, 192, 0.0)])
+def test_fused_verify_small(B, K, V, H, greedy):
+    rep = _fused_check(B, K, V, H, seed=B + V, greedy_frac=greedy)
+    if greedy == 1.0:
+        assert rep.sampling == 0
+    if greedy == 0.0:
+        assert rep.greedy == 0
+
+
+def test_fused_verify_largest_vocabulary():
+    """The largest-vocabulary shape (B=256, K=3, V=151936, ragged num_draft,
+    25% greedy) with hidden size 1024."""
+    rep = _fused_check(256, 3, 151936, 1024, seed=4)
+    assert rep.greedy > 0 and rep.sampling > 0
