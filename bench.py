@@ -60,12 +60,15 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--mode", choices=["chain", "typical", "tree", "early_exit"], default="chain",
+    ap.add_argument("--mode", choices=["chain", "typical", "tree", "early_exit", "lmhead"], default="chain",
                     help="chain: the lossless / greedy verifier (the headline line); "
                          "typical: typical acceptance on the same workload; tree: "
                          "token-tree verification of tries with --tree-nodes nodes; "
                          "early_exit: the verifier that stops reading a request's rows at "
-                         "its first rejection, timed beside the all-rows verifier")
+                         "its first rejection, timed beside the all-rows verifier; lmhead: "
+                         "the verifier fed with hidden states (the fused tcgen05 LM-head "
+                         "projection), timed beside separate projections")
+    ap.add_argument("--hidden", type=int, default=4096, help="hidden size H of --mode lmhead")
     ap.add_argument("--threshold", type=float, default=0.01, help="typical acceptance threshold")
     ap.add_argument("--tree-nodes", type=int, default=16)
     return ap.parse_args()
@@ -503,6 +506,128 @@ def run_early_exit(args, rank, world, local):
         torch.distributed.destroy_process_group()
 
 
+def run_lmhead(args, rank, world, local):
+    """The fused logits producer: the verifier fed with the target's hidden
+    states and LM head (spec_verify_lmhead), against the same verification
+    fed with logits from a separate projection (this library's tcgen05 GEMM,
+    or cuBLAS through torch.matmul), L2 flushed before every timed call."""
+    from speculative_decoding_verification_51_gb300 import binding
+    from speculative_decoding_verification_51_gb300 import build as _build
+    from speculative_decoding_verification_51_gb300 import workloads as W
+    from speculative_decoding_verification_51_gb300 import sharding
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+    binding.lib()
+    spec = W.SPECS[args.config]
+    B, K, V, H = spec.B, spec.K, spec.V, args.hidden
+    w = W.make_lmhead_workload(B, K, V, H, seed=args.config, ragged=args.config != 3,
+                               device=dev)
+    offset = sharding.weak_offset(rank, B)
+    n = w.num_draft.long()
+    pos = int(n.sum())
+    rows = int((n + 1).sum())
+    K1 = K + 1
+    ws = torch.empty(binding.lib().spec_verify_lmhead_workspace_size(B, K, V, H),
+                     dtype=torch.uint8, device=dev)
+    logits = torch.empty((B, K1, V), dtype=torch.bfloat16, device=dev)
+    out_ids = torch.empty((B, K1), dtype=torch.int32, device=dev)
+    out_nacc = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws2 = binding.new_workspace(B, K, V, dev)
+    # the listed rows' hidden states, for the projection-only timings
+    valid = (torch.arange(K1, device=dev)[None, :] <= n.to(dev)[:, None]).reshape(-1)
+    hid_rows = w.hidden.reshape(B * K1, H)[valid].contiguous()
+    lg_rows = torch.empty((rows, V), dtype=torch.bfloat16, device=dev)
+    hid_all = w.hidden.reshape(B * K1, H)
+    lg_all = logits.reshape(B * K1, V)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2(i):
+        flush.fill_(i & 0xFF)
+        flush_rd.sum()
+
+    def fused(seed):
+        binding.spec_verify_lmhead(w.hidden, w.lm_head, w.draft_probs, w.draft_ids, w.num_draft,
+                                   w.temperature, seed, logits_out=logits, out_ids=out_ids,
+                                   out_num_accepted=out_nacc, workspace=ws,
+                                   request_offset=offset)
+
+    def gemm_ours(seed):
+        binding.lmhead_logits(hid_rows, w.lm_head, out=lg_rows)
+
+    def gemm_cublas(seed):
+        torch.matmul(hid_rows, w.lm_head.T, out=lg_rows)
+
+    def two_step_cublas(seed):  # an engine's unfused step: project every row, then verify
+        torch.matmul(hid_all, w.lm_head.T, out=lg_all)
+        binding.spec_verify(logits, w.draft_probs, w.draft_ids, w.num_draft, w.temperature, seed,
+                            out_ids=out_ids, out_num_accepted=out_nacc, workspace=ws2,
+                            request_offset=offset)
+
+    variants = {"fused": fused, "gemm_ours": gemm_ours, "gemm_cublas": gemm_cublas,
+                "two_step_cublas": two_step_cublas}
+    for i in range(args.warmup):
+        for f in variants.values():
+            flush_l2(i)
+            f(1000 + i)
+    torch.cuda.synchronize()
+    evs = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)] for k in variants}
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        for i in range(args.steps):
+            for k, f in variants.items():
+                flush_l2(i + 7)
+                evs[k][i][0].record(stream)
+                f(2000 + i)
+                evs[k][i][1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = {k: sharding.max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e), device=dev)
+          for k, e in evs.items()}
+    flops = 2.0 * rows * V * H
+    d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = float(d.get("bf16_tflops", 1900.0))
+    tf_fused = flops / (ms["fused"] * 1e-3) / 1e12
+    tf_ours = flops / (ms["gemm_ours"] * 1e-3) / 1e12
+    tf_cublas = flops / (ms["gemm_cublas"] * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": world * pos / (ms["fused"] * 1e-3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms["fused"], 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 x bf16 -> f32 (projection); f32 (verification)",
+        "data": "synthetic", "mode": "lmhead",
+        "config": {"workload": f"{workload_name(args.config, None)} shapes (B={B}, K={K}, "
+                               f"V={V}) fed as hidden states, H={H}, integer operands",
+                   "rows_projected": rows, "positions_per_step": pos,
+                   "l2": "flushed before every timed call: 256 MiB write, then 256 MiB read"},
+        "ms": {k: round(v, 5) for k, v in ms.items()},
+        "tflops": {"fused_whole_call": round(tf_fused, 1), "gemm_ours": round(tf_ours, 1),
+                   "gemm_cublas": round(tf_cublas, 1)},
+        "speedup_fused_vs_two_step_cublas": round(ms["two_step_cublas"] / ms["fused"], 4),
+        "roofline": {"bound": "tensor", "achieved": round(tf_fused, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tf_fused / peak, 4), "traffic": None,
+                     "kernel": "whole fused call (projection of the listed rows)",
+                     "algorithmic_flops_per_launch": flops,
+                     "peak_kind": "measured (cuBLAS bf16 burst)"},
+        "gpu_launches": 5 * args.steps, "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -511,6 +636,9 @@ def main():
         return
     if args.mode == "early_exit":
         run_early_exit(args, rank, world, local)
+        return
+    if args.mode == "lmhead":
+        run_lmhead(args, rank, world, local)
         return
     if args.mode != "chain":
         run_variant(args, rank, world, local)

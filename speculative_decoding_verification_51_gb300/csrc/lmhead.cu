@@ -22,11 +22,12 @@
 // chunk) the maximum and, for sampling rows, the sum of 2^(l*kappa - c)
 // against c = RN(chunk max * kappa) (kept online over the chunk's 32-column
 // pieces, rescaled when the maximum grows), or for greedy rows the lowest
-// index of the maximum; l(x_j) and q(x_j) for the draft token; then the
-// per-request tile count and, by the warp that completes a request, its
-// acceptance (accept_request).  All of it is computed from the bf16-rounded
-// logits that are stored, so the later residual and bonus draws see the
-// same values.
+// index of the maximum; l(x_j) and q(x_j) for the draft token.  All of it
+// is computed from the bf16-rounded logits that are stored, so the later
+// residual and bonus draws see the same values.  k_accept_all then runs
+// every request's acceptance (accept_request), one warp per request: run by
+// the epilogue warps themselves, a warp that completed several requests at
+// once ran their acceptances one after another at the end of the GEMM.
 //
 // Every wait is bounded: a CTA that times out sets SPEC_BADBIT_TIMEOUT, lets
 // its copies and MMAs in flight finish (again bounded), frees its TMEM and
@@ -150,7 +151,9 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int chunk = blockIdx.x, mt = blockIdx.y;
+    // the row tiles of one 2048-column block run side by side, so its slice
+    // of the LM head is read from HBM once and then served from L2
+    const int mt = blockIdx.x, chunk = blockIdx.y;
     const int row0 = mt * LM_BM;
     const int rows = FUSED ? P.hdr[HDR_ROWS] : L.rows;  // fused: the rows k_plan listed
     if (row0 >= rows) return;  // whole CTA, before any barrier or TMEM
@@ -373,24 +376,6 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                     P.part[(size_t)slot * P.C + chunk] = o;
                     if (x >= 0) P.gath[slot] = make_float2(lx, qx);
                 }
-                __threadfence();  // this thread's partial before the counts
-                __syncwarp();
-                // one count per request among this warp's rows; the warp whose
-                // count completes (n_b + 1) * C runs the request's acceptance
-                const unsigned same = __match_any_sync(0xffffffffu, valid ? b : -1);
-                int done_b = 0;
-                if (valid && __ffs(same) - 1 == lane) {
-                    const int cnt = __popc(same);
-                    done_b = atomicAdd(&P.cnt[b], cnt) + cnt == (n + 1) * P.C;
-                }
-                unsigned todo = __ballot_sync(0xffffffffu, done_b);
-                while (todo) {
-                    const int l = __ffs(todo) - 1;
-                    todo &= todo - 1;
-                    const int bb = __shfl_sync(0xffffffffu, b, l);
-                    __threadfence();  // every other warp's partials after the count
-                    accept_request(P, bb);
-                }
             }
         }
     }
@@ -403,6 +388,13 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                      "r"(LM_TMEM_COLS)
                      : "memory");
     if (threadIdx.x == 0 && *abort_v) atomicOr(L.status, int(SPEC_BADBIT_TIMEOUT));
+}
+
+// The acceptance of every valid request, one warp each, once all its row
+// statistics exist (the fused projection has finished).
+__global__ void __launch_bounds__(256) k_accept_all(Params P) {
+    const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (b < P.B && P.req_flags[b] == 0) accept_request(P, b);
 }
 
 // The listed rows' hidden states, in list order (one warp per row, 16-byte
@@ -497,8 +489,9 @@ spec_status launch_lmhead_fused(const Params& P, const LmHeadIn& in, cudaStream_
     L.V = P.V;
     L.out = static_cast<uint16_t*>(const_cast<void*>(P.logits));
     L.status = P.status;
-    const dim3 grid(unsigned(P.C), unsigned((maxrows + LM_BM - 1) / LM_BM));
+    const dim3 grid(unsigned((maxrows + LM_BM - 1) / LM_BM), unsigned(P.C));
     k_lmhead<true><<<grid, LM_THREADS, LM_SMEM, st>>>(ma, mb, L, P);
+    k_accept_all<<<(P.B + 7) / 8, 256, 0, st>>>(P);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
@@ -529,7 +522,7 @@ spec_status spec_lmhead_logits(const void* hidden, const void* lm_head, int rows
     L.out = static_cast<uint16_t*>(logits_out);
     L.status = dev_status;
     Params P = {};
-    const dim3 grid(unsigned((V + TILE - 1) / TILE), unsigned((rows + LM_BM - 1) / LM_BM));
+    const dim3 grid(unsigned((rows + LM_BM - 1) / LM_BM), unsigned((V + TILE - 1) / TILE));
     k_lmhead<false><<<grid, LM_THREADS, LM_SMEM, reinterpret_cast<cudaStream_t>(stream)>>>(ma, mb,
                                                                                            L, P);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
