@@ -341,7 +341,10 @@ __global__ void k_emit_bf16(Params P);
 
 __global__ void k_tree_walk_f32(Params P);
 __global__ void k_tree_walk_bf16(Params P);
-constexpr int TREE_THREADS = 256;
+#ifndef SV_TREE_THREADS
+#define SV_TREE_THREADS 256
+#endif
+constexpr int TREE_THREADS = SV_TREE_THREADS;
 constexpr int TREE_MAX_NODES = 32;
 
 __global__ void k_philox_fill(uint64_t seed, const uint32_t* ctrs, int64_t n, uint32_t* out);

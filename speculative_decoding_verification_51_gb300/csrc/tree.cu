@@ -36,6 +36,11 @@ namespace {
 
 constexpr int TW = TREE_THREADS / 32;  // warps per CTA
 constexpr int GROUPS = TILE / 8 / 32;  // 8-token groups per lane in a chunk
+#ifndef SV_TREE_BATCH
+#define SV_TREE_BATCH 4
+#endif
+constexpr int PASS_BATCH = SV_TREE_BATCH;  // groups of a pass whose loads are issued together
+static_assert(GROUPS % PASS_BATCH == 0, "whole batches of groups per chunk");
 
 template <int DT>
 __device__ __forceinline__ void logits8(const Params& P, size_t row_base, int y0, float (&l)[8]) {
@@ -277,7 +282,46 @@ __device__ __forceinline__ void tree_walk_body(const Params& P) {
             // rejected: S = sum_y max(0, r_k(y) - q_c(y)), and its chunk masses
             const int k = s_ch.n;
             double part = 0.0;
-            for (int ch = warp; ch < P.C; ch += TW) {
+            for (int ch = warp; ch < P.C && k == 0; ch += TW) {
+                // first rejection at this node: r = p, so each group needs its
+                // logits and one q row; PASS_BATCH groups' loads are issued
+                // before their arithmetic (same operations, same order)
+                const int y_end = min(TILE, P.V - ch * TILE);
+                const float* qrow = s_qrows[0];
+                float acc_f = 0.f;
+#pragma unroll 1
+                for (int g0 = 0; g0 < GROUPS; g0 += PASS_BATCH) {
+                    float l[PASS_BATCH][8], q[PASS_BATCH][8];
+#pragma unroll
+                    for (int u = 0; u < PASS_BATCH; ++u) {
+                        const int gl = (g0 + u) * 32 + lane;
+                        if (gl * 8 < y_end) {
+                            logits8<DT>(P, vbase, ch * TILE + gl * 8, l[u]);
+                            probs8(qrow, ch * TILE + gl * 8, q[u]);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < PASS_BATCH; ++u) {
+                        const int gl = (g0 + u) * 32 + lane;
+                        if (gl * 8 >= y_end) continue;
+                        float r[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float pe = __fmul_rn(ex2_approx(weight_arg(l[u][e], m, cv, kappa)), invZ);
+                            r[e] = fmaxf(__fsub_rn(pe, q[u][e]), 0.f);
+                        }
+#pragma unroll
+                        for (int h = 4; h; h >>= 1)
+#pragma unroll
+                            for (int e = 0; e < h; ++e) r[e] = __fadd_rn(r[e], r[e + h]);
+                        acc_f = __fadd_rn(acc_f, r[0]);
+                    }
+                }
+                const float cm = warp_sum_f(acc_f);
+                if (lane == 0) P.tmass[(size_t)b * P.C + ch] = cm;
+                part += double(cm);
+            }
+            for (int ch = warp; ch < P.C && k > 0; ch += TW) {
                 const int y_end = min(TILE, P.V - ch * TILE);
                 float acc_f = 0.f;
 #pragma unroll 1
