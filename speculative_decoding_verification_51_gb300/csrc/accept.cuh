@@ -62,7 +62,11 @@ __device__ __forceinline__ void merge_argmax(float& m, int& a, float m2, int a2)
 }  // namespace
 
 // Request b (valid: k_plan has checked num_draft and temperature); whole warp.
-static __device__ __noinline__ void accept_request(const Params& P, int b) {
+// n = num_draft[b] and kappa = log2(e) / T (0 for greedy) are passed in by the
+// caller, which already holds them, so the acceptance starts with the loads
+// that depend on nothing else.
+static __device__ __noinline__ void accept_request(const Params& P, int b, int n, bool greedy,
+                                                   float kappa) {
     const int lane = threadIdx.x & 31;
     const int K1 = P.K1;
     int32_t* out = P.out_ids + (size_t)b * K1;
@@ -85,11 +89,6 @@ static __device__ __noinline__ void accept_request(const Params& P, int b) {
             }
         }
     };
-
-    const int n = P.num_draft[b];
-    const float T = P.temp[b];
-    const bool greedy = (T == 0.f);
-    const float kappa = greedy ? 0.f : kappa_of(T);
 
     // rows jlo..jhi are in this pass: all of them, or one early-exit round's
     const bool ee = P.round >= 0;

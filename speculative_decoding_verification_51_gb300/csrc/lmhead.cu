@@ -446,7 +446,10 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
 // statistics exist (the fused projection has finished).
 __global__ void __launch_bounds__(256) k_accept_all(Params P) {
     const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (b < P.B && P.req_flags[b] == 0) accept_request(P, b);
+    if (b < P.B && P.req_flags[b] == 0) {
+        const float T = P.temp[b];
+        accept_request(P, b, P.num_draft[b], T == 0.f, T == 0.f ? 0.f : kappa_of(T));
+    }
 }
 
 // The listed rows' hidden states, in list order (one warp per row, 16-byte

@@ -189,6 +189,8 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
 
     // the run of consecutive tiles of one request that this warp has finished
     int seg_b = rc.b, seg_n = rc.n, seg_tiles = 0;
+    bool seg_greedy = rc.greedy;
+    float seg_kappa = rc.kappa;
     auto flush = [&]() {
         int last = 0;
         if (lane == 0 && seg_tiles > 0 && !P.tree) {  // trees are walked by k_tree_walk
@@ -200,7 +202,7 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
         }
         if (__shfl_sync(0xffffffffu, last, 0)) {
             __threadfence();  // every other warp's partials after the count
-            accept_request(P, seg_b);
+            accept_request(P, seg_b, seg_n, seg_greedy, seg_kappa);
         }
         seg_tiles = 0;
     };
@@ -329,6 +331,8 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
                     flush();
                     seg_b = rc.b;
                     seg_n = rc.n;
+                    seg_greedy = rc.greedy;
+                    seg_kappa = rc.kappa;
                 }
             }
         }
