@@ -97,3 +97,54 @@ def test_typical_host_side_errors(lib):
     assert call(0.1, V=1020) == bd.SPEC_ERR_UNSUPPORTED
     assert call(0.1, B=0) == bd.SPEC_OK
     assert call(float("inf"), ws=0x80010) == bd.SPEC_ERR_WORKSPACE
+
+
+def test_early_exit_host_side_errors(lib):
+    """spec_verify_early_exit checks as spec_verify_ex does, plus seed_dev alignment."""
+    from speculative_decoding_verification_51_gb300 import binding as bd
+    vp = ctypes.c_void_p
+
+    def call(B=2, K=3, V=64, seed_dev=None, ws=0x80000):
+        return lib.spec_verify_early_exit(vp(0x10000), 1, vp(0x20000), vp(0x30000), vp(0x40000),
+                                          vp(0x50000), ctypes.c_uint64(0), B, K, V, vp(0x60000),
+                                          vp(0x70000), vp(ws), 1 << 30, vp(0), ctypes.c_uint32(0),
+                                          None, None, None, None if seed_dev is None else vp(seed_dev))
+    assert call(K=32) == bd.SPEC_ERR_INVALID_ARG
+    assert call(V=1020) == bd.SPEC_ERR_UNSUPPORTED
+    assert call(B=0) == bd.SPEC_OK
+    assert call(seed_dev=0x90004) == bd.SPEC_ERR_INVALID_ARG   # not 8-byte aligned
+    assert call(ws=0x80010) == bd.SPEC_ERR_WORKSPACE
+
+
+def test_lmhead_host_side_errors(lib):
+    """spec_lmhead_logits / spec_verify_lmhead reject bad sizes and pointers
+    before any launch."""
+    from speculative_decoding_verification_51_gb300 import binding as bd
+    vp = ctypes.c_void_p
+
+    def proj(rows=4, H=64, V=64, hid=0x10000, w=0x20000, out=0x30000, st=0x40000):
+        return lib.spec_lmhead_logits(vp(hid), vp(w), rows, H, V, vp(out), vp(st), vp(0))
+    assert proj(H=96) == bd.SPEC_ERR_UNSUPPORTED      # H not a multiple of 64
+    assert proj(V=1020) == bd.SPEC_ERR_UNSUPPORTED    # V not a multiple of 8
+    assert proj(H=0) == bd.SPEC_ERR_INVALID_ARG
+    assert proj(rows=-1) == bd.SPEC_ERR_INVALID_ARG
+    assert proj(rows=0) == bd.SPEC_OK
+    assert proj(hid=0) == bd.SPEC_ERR_INVALID_ARG
+    assert proj(st=0) == bd.SPEC_ERR_INVALID_ARG
+    assert proj(w=0x20008) == bd.SPEC_ERR_UNSUPPORTED  # not 16-byte aligned
+
+    assert lib.spec_verify_lmhead_workspace_size(4, 3, 64, 96) == 0
+    n = lib.spec_verify_lmhead_workspace_size(4, 3, 64, 128)
+    assert n >= lib.spec_verify_workspace_size(4, 3, 64) + 4 * 4 * 128 * 2
+
+    def fused(B=4, K=3, V=64, H=128, hid=0x10000, ws_bytes=None):
+        return lib.spec_verify_lmhead(vp(hid), vp(0x20000), H, vp(0x30000), vp(0x40000),
+                                      vp(0x50000), vp(0x60000), vp(0x70000), ctypes.c_uint64(0),
+                                      B, K, V, vp(0x80000), vp(0x90000), vp(0x100000),
+                                      n if ws_bytes is None else ws_bytes, vp(0),
+                                      ctypes.c_uint32(0), None, None, None)
+    assert fused(H=96) == bd.SPEC_ERR_UNSUPPORTED
+    assert fused(K=32) == bd.SPEC_ERR_INVALID_ARG
+    assert fused(B=0) == bd.SPEC_OK
+    assert fused(hid=0) == bd.SPEC_ERR_INVALID_ARG
+    assert fused(ws_bytes=n - 1) == bd.SPEC_ERR_WORKSPACE
