@@ -342,7 +342,7 @@ __global__ void k_emit_bf16(Params P);
 __global__ void k_tree_walk_f32(Params P);
 __global__ void k_tree_walk_bf16(Params P);
 #ifndef SV_TREE_THREADS
-#define SV_TREE_THREADS 256
+#define SV_TREE_THREADS 512
 #endif
 constexpr int TREE_THREADS = SV_TREE_THREADS;
 constexpr int TREE_MAX_NODES = 32;
