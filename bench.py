@@ -363,7 +363,7 @@ def run_variant(args, rank, world, local):
     ms = sharding.max_over_ranks(ms, device=dev)
     peak, peak_kind, _ = measured_peak()
     gbs = algo / (ms * 1e-3) / 1e9
-    n_kernels = 3 if args.mode == "tree" else 4
+    n_kernels = 3 if args.mode == "tree" else 5  # tree: plan, row stats, walk
     line = {
         "metric": METRIC, "value": world * pos / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -498,7 +498,9 @@ def run_early_exit(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(gbs / peak, 4), "traffic": None, "kernel": "whole call",
                      "algorithmic_bytes_per_launch": algo_ee, "peak_kind": peak_kind},
-        "gpu_launches": (K + 4) * args.steps, "clocks": clk.summary(),
+        # early exit: plan, K + 1 passes, sample, emit; all rows: plan, row
+        # stats, accept, sample, emit
+        "gpu_launches": (K + 4 + 5) * args.steps, "clocks": clk.summary(),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -620,7 +622,9 @@ def run_lmhead(args, rank, world, local):
                      "kernel": "whole fused call (projection of the listed rows)",
                      "algorithmic_flops_per_launch": flops,
                      "peak_kind": "measured (cuBLAS bf16 burst)"},
-        "gpu_launches": 5 * args.steps, "clocks": clk.summary(),
+        # fused: plan, gather, projection, accept, sample, emit; projection
+        # alone: 1; cuBLAS + spec_verify: the five verification kernels
+        "gpu_launches": (6 + 1 + 5) * args.steps, "clocks": clk.summary(),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -326,9 +326,9 @@ spec_status spec_verify_tree(const void* target_logits, spec_dtype logits_dtype,
 
 /*
  * spec_verify_profiled -- spec_verify with timing marks: the caller's CUDA
- * events events[0..4] (cudaEvent_t) are recorded on `stream` before each of
- * the four kernels of the call (plan; row statistics with the acceptance
- * tests; residual masses; sampled tokens) and after the last, so that
+ * events events[0..5] (cudaEvent_t) are recorded on `stream` before each of
+ * the five kernels of the call (plan; row statistics; acceptance tests;
+ * residual masses; sampled tokens) and after the last, so that
  * events[i] -> events[i+1] brackets kernel i.
  * The marks separate the kernels, which otherwise overlap their launch with
  * the previous kernel's tail.  Returns SPEC_ERR_INVALID_ARG if any event is

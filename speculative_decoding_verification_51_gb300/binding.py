@@ -22,7 +22,7 @@ BADBIT = {"num_draft": 1, "temperature": 2, "draft_id": 4, "empty_row": 8, "no_p
           "timeout": 32, "tree": 64}
 MODE_BAD, MODE_GREEDY, MODE_RESIDUAL, MODE_BONUS, MODE_FALLBACK, MODE_TYPICAL = -1, 0, 1, 2, 3, 4
 MAX_K = 31
-KERNELS = ("k_plan", "k_row_stats", "k_sample", "k_emit")  # launch order
+KERNELS = ("k_plan", "k_row_stats", "k_accept_all", "k_sample", "k_emit")  # launch order
 N_KERNELS = len(KERNELS)
 
 _LOCK = threading.Lock()

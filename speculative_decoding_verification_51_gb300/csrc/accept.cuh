@@ -1,11 +1,13 @@
-// accept.cuh -- acceptance of one request by one warp, run inside k_row_stats
-// by the warp that completes the request's last (row, chunk) tile.
+// accept.cuh -- acceptance of one request by one warp: in k_accept_all (one
+// warp per request) once the all-rows pass or the fused projection has
+// written every row statistic, and inside k_row_stats, by the warp that
+// completes a request's row, in an early-exit pass.
 //
 // Lane j owns row j of the request.  Steps (pages cited by title / section):
 //   1. merge the chunk partials of every row j <= n_b into the row's max m_j,
 //      normaliser Z_j = sum_x 2^((l_j(x) - m_j) kappa) and, for greedy rows,
-//      the lowest-index argmax (all partial loads issued before any merge;
-//      float32 throughout: the FP64 pipe of this part is slow);
+//      the lowest-index argmax (merge_row: one warp per row, float32
+//      throughout: the FP64 pipe of this part is slow);
 //   2. acceptance of draft x_j ("深入推测解码" 保证原始分布 step 3,
 //      "RTP-LLM Speculative Engine" 拒绝采样算法): p = 2^((l_j(x_j) - m_j) kappa)
 //      / Z_j with l_j(x_j) and q_j(x_j) gathered by k_row_stats, u_j = Philox
@@ -26,8 +28,8 @@
 // draft is written out and row r + 1 joins the list of the next round;
 // otherwise the request ends here with a_b = r, exactly as the all-rows pass
 // would have ended it.
-// Values written by other warps during the same kernel (partials, gathered
-// logits) are read through L2 (ld.global.cg), after the caller's fence.
+// Partials and gathers written by other warps are read through L2
+// (ld.global.cg): after the caller's fence (early exit) or in the next kernel.
 #pragma once
 
 #include <cfloat>
@@ -61,16 +63,117 @@ __device__ __forceinline__ void merge_argmax(float& m, int& a, float m2, int a2)
 
 }  // namespace
 
-// Request b (valid: k_plan has checked num_draft and temperature); whole warp.
-// n = num_draft[b] and kappa = log2(e) / T (0 for greedy) are passed in by the
-// caller, which already holds them, so the acceptance starts with the loads
-// that depend on nothing else.
-static __device__ __noinline__ void accept_request(const Params& P, int b, int n, bool greedy,
-                                                   float kappa) {
+// The per-lane inputs of the acceptance that depend on nothing merged: the
+// draft token, its gathered {l_j(x_j), q_j(x_j)} and the Philox block of the
+// lane's row (rows jlo..jhi of request b).
+struct AccLoads {
+    int x;
+    float2 g;
+    uint4 rb;
+};
+
+__device__ __forceinline__ AccLoads accept_loads(const Params& P, int b, int n, bool greedy,
+                                                 int jlo, int jhi) {
+    const int lane = threadIdx.x & 31;
+    const bool row_lane = lane >= jlo && lane <= jhi;
+    const bool draft_lane = row_lane && lane < n;
+    AccLoads L;
+    L.x = draft_lane ? P.ids[(size_t)b * P.K + lane] : -1;
+    L.g = make_float2(0.f, 0.f);
+    if (draft_lane && !greedy) L.g = __ldcg(P.gath + (size_t)b * P.K1 + lane);
+    L.rb = make_uint4(0, 0, 0, 0);
+    if (!greedy && row_lane) L.rb = row_block(P, b, lane);
+    return L;
+}
+
+// Step 1 for one row (whole warp; every lane gets the result): M = the row
+// max, Z = its normaliser against RN(M kappa), A = the lowest index of the
+// max (greedy rows).  With at most 128 chunks a lane's chunks stay in
+// registers: the max first (shuffles), then every chunk rebased onto it once
+// (one ex2 each) and summed (shuffles); longer rows merge pairwise.
+__device__ __forceinline__ void merge_row(const Partial* prow, int C, bool greedy, float kappa,
+                                          float& M, float& Z, int& A) {
+    const int lane = threadIdx.x & 31;
+    constexpr int NPL = 4;  // chunks per lane held in registers
+    if (C <= 32 * NPL) {
+        Partial q[NPL];
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+            const int c = lane + 32 * i;
+            if (c < C) {
+                const double2 raw = __ldcg(reinterpret_cast<const double2*>(prow + c));
+                q[i] = *reinterpret_cast<const Partial*>(&raw);
+            } else {
+                q[i].m = -INFINITY;
+                q[i].amax = INT_MAX;
+                q[i].z = 0.0;
+            }
+        }
+        float lm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) lm = fmaxf(lm, q[i].m);
+        M = warp_max(lm);
+        A = INT_MAX;
+        Z = 0.f;
+        if (greedy) {
+            int la = INT_MAX;
+#pragma unroll
+            for (int i = 0; i < NPL; ++i)
+                if (q[i].m == M) la = min(la, q[i].amax);
+            A = warp_min_int(la);
+        } else {
+            float lz = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < NPL; ++i)
+                    if (q[i].m != -INFINITY && q[i].z != 0.0)
+                        lz = fmaf(float(q[i].z), ex2_approx(rebase_arg(q[i].m, M, kappa)), lz);
+            }
+            Z = warp_sum_f(lz);
+        }
+    } else {  // long vocabularies: pairwise merges over the lane's chunks
+        float m = -INFINITY;
+        int am = INT_MAX;
+        float z = 0.f;
+        for (int c = lane; c < C; c += 32) {
+            const double2 raw = __ldcg(reinterpret_cast<const double2*>(prow + c));
+            const Partial q = *reinterpret_cast<const Partial*>(&raw);
+            if (greedy)
+                merge_argmax(m, am, q.m, q.amax);
+            else
+                merge_sum(m, z, q.m, float(q.z), kappa);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float om = __shfl_xor_sync(0xffffffffu, m, o);
+            if (greedy)
+                merge_argmax(m, am, om, __shfl_xor_sync(0xffffffffu, am, o));
+            else
+                merge_sum(m, z, om, __shfl_xor_sync(0xffffffffu, z, o), kappa);
+        }
+        M = m;
+        A = am;
+        Z = z;
+    }
+}
+
+// Steps 2-4 of request b (whole warp; lane j holds row j's merged M, Z, A for
+// jlo <= j <= jhi).  n = num_draft[b], kappa = log2(e) / T (0 for greedy).
+static __device__ __noinline__ void accept_decide(const Params& P, int b, int n, bool greedy,
+                                                  float kappa, const AccLoads& L, float my_m,
+                                                  int my_amax, float my_Z) {
     const int lane = threadIdx.x & 31;
     const int K1 = P.K1;
     int32_t* out = P.out_ids + (size_t)b * K1;
     const float NaN = __int_as_float(0x7fc00000);
+    const bool ee = P.round >= 0;
+    const int jlo = ee ? P.round : 0, jhi = ee ? P.round : n;
+    const bool row_lane = lane >= jlo && lane <= jhi;
+    const bool draft_lane = row_lane && lane < n;
+    const int x = L.x;
+    const float2 g = L.g;
+    const uint4 rb = L.rb;
+    const bool typical = P.rule == RULE_TYPICAL;
 
     auto fail = [&](int flags) {
         if (lane < K1) out[lane] = -1;
@@ -89,109 +192,6 @@ static __device__ __noinline__ void accept_request(const Params& P, int b, int n
             }
         }
     };
-
-    // rows jlo..jhi are in this pass: all of them, or one early-exit round's
-    const bool ee = P.round >= 0;
-    const int jlo = ee ? P.round : 0, jhi = ee ? P.round : n;
-    const bool row_lane = lane >= jlo && lane <= jhi;
-
-    // loads that do not depend on the merge go first
-    const bool draft_lane = row_lane && lane < n;
-    const int x = draft_lane ? P.ids[(size_t)b * P.K + lane] : -1;
-    float2 g = make_float2(0.f, 0.f);
-    if (draft_lane && !greedy) g = __ldcg(P.gath + (size_t)b * K1 + lane);
-    const bool typical = P.rule == RULE_TYPICAL;
-    uint4 rb = make_uint4(0, 0, 0, 0);
-    if (!greedy && row_lane) rb = row_block(P, b, lane);
-
-    // 1. per-row merge, four rows at a time; lane j keeps row j.  With at most
-    // 128 chunks per row a lane's chunks stay in registers: the row max first
-    // (shuffles), then every chunk rebased onto it once (one ex2 each) and
-    // summed (shuffles); greedy rows take the lowest index attaining the max.
-    float my_m = -INFINITY;
-    int my_amax = INT_MAX;
-    float my_Z = 0.f;
-    const Partial* pb = P.part + (size_t)b * K1 * P.C;
-    constexpr int NPL = 4;  // chunks per lane held in registers
-    if (P.C <= 32 * NPL) {
-        for (int j0 = jlo; j0 <= jhi; j0 += 4) {
-            Partial q[4][NPL];
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-                for (int i = 0; i < NPL; ++i) {
-                    const int c = lane + 32 * i;
-                    if (j0 + jj <= jhi && c < P.C) {
-                        const double2 raw = __ldcg(reinterpret_cast<const double2*>(
-                            pb + (size_t)(j0 + jj) * P.C + c));
-                        q[jj][i] = *reinterpret_cast<const Partial*>(&raw);
-                    } else {
-                        q[jj][i].m = -INFINITY;
-                        q[jj][i].amax = INT_MAX;
-                        q[jj][i].z = 0.0;
-                    }
-                }
-#pragma unroll 1
-            for (int jj = 0; jj < 4; ++jj) {
-                if (j0 + jj > jhi) break;
-                float lm = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < NPL; ++i) lm = fmaxf(lm, q[jj][i].m);
-                const float M = warp_max(lm);
-                int A = INT_MAX;
-                float Z = 0.f;
-                if (greedy) {
-                    int la = INT_MAX;
-#pragma unroll
-                    for (int i = 0; i < NPL; ++i)
-                        if (q[jj][i].m == M) la = min(la, q[jj][i].amax);
-                    A = warp_min_int(la);
-                } else {
-                    float lz = 0.f;
-                    if (M != -INFINITY) {
-#pragma unroll
-                        for (int i = 0; i < NPL; ++i)
-                            if (q[jj][i].m != -INFINITY && q[jj][i].z != 0.0)
-                                lz = fmaf(float(q[jj][i].z), ex2_approx(rebase_arg(q[jj][i].m, M, kappa)), lz);
-                    }
-                    Z = warp_sum_f(lz);
-                }
-                if (lane == j0 + jj) {
-                    my_m = M;
-                    my_amax = A;
-                    my_Z = Z;
-                }
-            }
-        }
-    } else {  // long vocabularies: pairwise merges over the lane's chunks
-        for (int j = jlo; j <= jhi; ++j) {
-            float m = -INFINITY;
-            int am = INT_MAX;
-            float z = 0.f;
-            for (int c = lane; c < P.C; c += 32) {
-                const double2 raw =
-                    __ldcg(reinterpret_cast<const double2*>(pb + (size_t)j * P.C + c));
-                const Partial q = *reinterpret_cast<const Partial*>(&raw);
-                if (greedy)
-                    merge_argmax(m, am, q.m, q.amax);
-                else
-                    merge_sum(m, z, q.m, float(q.z), kappa);
-            }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) {
-                const float om = __shfl_xor_sync(0xffffffffu, m, o);
-                if (greedy)
-                    merge_argmax(m, am, om, __shfl_xor_sync(0xffffffffu, am, o));
-                else
-                    merge_sum(m, z, om, __shfl_xor_sync(0xffffffffu, z, o), kappa);
-            }
-            if (lane == j) {
-                my_m = m;
-                my_amax = am;
-                my_Z = z;
-            }
-        }
-    }
 
     // 2. validation of the draft ids and rows this request uses
     const unsigned bad_id = __ballot_sync(0xffffffffu, draft_lane && (x < 0 || x >= P.V));
@@ -285,6 +285,31 @@ static __device__ __noinline__ void accept_request(const Params& P, int b, int n
         d[1] = float(a);
         d[2] = d[3] = NaN;
     }
+}
+
+// Request b in an early-exit pass (valid: k_plan has checked num_draft and
+// temperature); whole warp.  n and kappa come from the caller, which already
+// holds them.
+static __device__ __noinline__ void accept_request(const Params& P, int b, int n, bool greedy,
+                                                   float kappa) {
+    const int lane = threadIdx.x & 31;
+    const bool ee = P.round >= 0;
+    const int jlo = ee ? P.round : 0, jhi = ee ? P.round : n;
+    const AccLoads L = accept_loads(P, b, n, greedy, jlo, jhi);
+    float my_m = -INFINITY, my_Z = 0.f;
+    int my_amax = INT_MAX;
+    const Partial* pb = P.part + (size_t)b * P.K1 * P.C;
+    for (int j = jlo; j <= jhi; ++j) {
+        float M, Z;
+        int A;
+        merge_row(pb + (size_t)j * P.C, P.C, greedy, kappa, M, Z, A);
+        if (lane == j) {
+            my_m = M;
+            my_amax = A;
+            my_Z = Z;
+        }
+    }
+    accept_decide(P, b, n, greedy, kappa, L, my_m, my_amax, my_Z);
 }
 
 }  // namespace sv

@@ -221,14 +221,18 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
                        st, false, P);
         return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
     }
+    // the all-rows pass leaves the acceptances to one warp per request here
+    if (!lm && !early_exit && e == cudaSuccess)
+        e = launch(k_accept_all, unsigned(B), ACCEPT_WARPS * 32, 0, st, true, P);
+    if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess)
         e = launch(bf16 ? k_sample_bf16 : k_sample_f32, unsigned(g3), SAMPLE_WARPS * 32,
                    sample_smem(logits_dtype), st, true, P);
-    if (e == cudaSuccess) e = mark(3);
+    if (e == cudaSuccess) e = mark(4);
     if (e == cudaSuccess)
         e = launch(bf16 ? k_emit_bf16 : k_emit_f32, g4, SAMPLE_WARPS * 32,
                    sample_smem(logits_dtype) / 2, st, true, P);
-    if (e == cudaSuccess) e = mark(4);
+    if (e == cudaSuccess) e = mark(5);
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
@@ -371,7 +375,7 @@ spec_status spec_verify_profiled(const void* target_logits, spec_dtype logits_dt
                                  size_t workspace_bytes, spec_stream_t stream,
                                  spec_event_t* events) {
     if (!events) return SPEC_ERR_INVALID_ARG;
-    for (int i = 0; i < 5; ++i)
+    for (int i = 0; i < 6; ++i)
         if (!events[i]) return SPEC_ERR_INVALID_ARG;
     return verify_impl(target_logits, logits_dtype, draft_probs, draft_ids, num_draft,
                        temperature, seed, B, K, V, out_ids, out_num_accepted, workspace,

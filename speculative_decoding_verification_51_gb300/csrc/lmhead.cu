@@ -442,16 +442,6 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
     if (threadIdx.x == 0 && *abort_v) atomicOr(L.status, int(SPEC_BADBIT_TIMEOUT));
 }
 
-// The acceptance of every valid request, one warp each, once all its row
-// statistics exist (the fused projection has finished).
-__global__ void __launch_bounds__(256) k_accept_all(Params P) {
-    const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (b < P.B && P.req_flags[b] == 0) {
-        const float T = P.temp[b];
-        accept_request(P, b, P.num_draft[b], T == 0.f, T == 0.f ? 0.f : kappa_of(T));
-    }
-}
-
 // The listed rows' hidden states, in list order (one warp per row, 16-byte
 // copies); rows past the list are left as they are.
 __global__ void __launch_bounds__(256) k_gather_rows(Params P, LmHeadIn in) {
@@ -568,7 +558,7 @@ spec_status launch_lmhead_fused(const Params& P, const LmHeadIn& in, cudaStream_
     L.status = P.status;
     const dim3 grid(unsigned(pair_tiles(maxrows)), unsigned(P.C));
     if (launch_lm<true>(grid, st, ma, mb, L, P) != cudaSuccess) return SPEC_ERR_CUDA;
-    k_accept_all<<<(P.B + 7) / 8, 256, 0, st>>>(P);
+    k_accept_all<<<P.B, ACCEPT_WARPS * 32, 0, st>>>(P);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -26,11 +26,13 @@
 // No block-wide barrier and no float64 arithmetic (the FP64 pipe of this part
 // is a small fraction of its FP32 rate).  Output: one Partial per tile.
 //
-// Completion: each warp adds the number of tiles it finished for a request to
-// the request's counter (one atomic per contiguous run of that request's
-// tiles, after a threadfence); the warp whose addition completes the count
-// (n_b + 1) * C runs the request's acceptance (accept_request) at once.
-// Nothing ever waits for another warp.
+// Acceptance: after the all-rows pass, k_accept_all (one warp per request)
+// runs every request's acceptance (accept_request).  In an early-exit pass
+// each warp adds the number of tiles it finished for a request to the
+// request's counter (one atomic per contiguous run, after a threadfence) and
+// the warp whose addition completes the row runs the acceptance at once, so
+// that the survivors' next rows are listed before the next pass.  Nothing
+// ever waits for another warp.
 #include <cfloat>
 #include <climits>
 
@@ -191,9 +193,14 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
     int seg_b = rc.b, seg_n = rc.n, seg_tiles = 0;
     bool seg_greedy = rc.greedy;
     float seg_kappa = rc.kappa;
+    // Only early-exit passes count tiles here: the all-rows pass leaves every
+    // acceptance to k_accept_all, so its warps never stop streaming to fence
+    // and count (a warp whose range crossed a request boundary used to lose
+    // about 5 us there), and tree passes are walked by k_tree_walk.
+    const bool counting = P.round >= 0 && !P.tree;
     auto flush = [&]() {
         int last = 0;
-        if (lane == 0 && seg_tiles > 0 && !P.tree) {  // trees are walked by k_tree_walk
+        if (lane == 0 && seg_tiles > 0 && counting) {
             __threadfence();  // this warp's partials before its count
             // an early-exit request completes one row per round; its count
             // is never reset, so round r ends at (r + 1) * C
@@ -349,6 +356,42 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
         for (long long u = i; u < n_tiles && u < i + STATS_STAGES; ++u)
             mbar_wait_bounded(&bars[warp][int(u % STATS_STAGES)], uint32_t((u / STATS_STAGES) & 1),
                               100000000ull);
+    }
+}
+
+// The acceptance of every valid request once all its row statistics exist
+// (after the all-rows pass, or after the fused projection): one CTA per
+// request; its warps merge the request's rows side by side (warp w: rows w,
+// w + ACCEPT_WARPS, ...), then warp 0, whose own loads were issued first,
+// decides.
+__global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept_all(Params P) {
+    griddep_wait();  // the row statistics
+    const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (b >= P.B || P.req_flags[b] != 0) return;  // bad requests: k_plan wrote their outputs
+    __shared__ float s_m[SPEC_MAX_K + 1], s_z[SPEC_MAX_K + 1];
+    __shared__ int s_a[SPEC_MAX_K + 1];
+    const int n = P.num_draft[b];
+    const float T = P.temp[b];
+    const bool greedy = (T == 0.f);
+    const float kappa = greedy ? 0.f : kappa_of(T);
+    AccLoads L;
+    if (warp == 0) L = accept_loads(P, b, n, greedy, 0, n);
+    const Partial* pb = P.part + (size_t)b * P.K1 * P.C;
+    for (int j = warp; j <= n; j += ACCEPT_WARPS) {
+        float M, Z;
+        int A;
+        merge_row(pb + (size_t)j * P.C, P.C, greedy, kappa, M, Z, A);
+        if (lane == 0) {
+            s_m[j] = M;
+            s_z[j] = Z;
+            s_a[j] = A;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const bool mine = lane <= n;
+        accept_decide(P, b, n, greedy, kappa, L, mine ? s_m[lane] : -INFINITY,
+                      mine ? s_a[lane] : INT_MAX, mine ? s_z[lane] : 0.f);
     }
 }
 
