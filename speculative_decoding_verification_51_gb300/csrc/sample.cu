@@ -135,8 +135,10 @@ __device__ __forceinline__ double warp_incl_scan(double x) {
 }
 
 // Level 1 over nc chunk masses mass(c) in chunk order, by one warp: S = the
-// last prefix; the chosen chunk is the first whose prefix reaches u * S.
-// Up to 128 chunks are loaded at once (one round trip); beyond, block by block.
+// total; the chosen chunk is the first of positive mass whose prefix reaches
+// u * S (the last of positive mass if rounding leaves u * S beyond every
+// prefix).  Up to 128 chunks are loaded at once (one round trip) and summed
+// with one warp scan; beyond, block by block.
 template <typename MassFn>
 __device__ __forceinline__ Pick pick_chunk(int nc, float u, MassFn mass) {
     const int lane = threadIdx.x & 31;
@@ -145,28 +147,49 @@ __device__ __forceinline__ Pick pick_chunk(int nc, float u, MassFn mass) {
     pk.chunk = -1;
     pk.before = 0.0;
     if (nc <= NB * 32) {
-        double v[NB], incl[NB];
+        // lane l holds chunks NB*l .. NB*l + NB - 1, so chunk order runs lane
+        // by lane: one warp scan of the lane sums, then a walk within the lane
+        double v[NB];
 #pragma unroll
-        for (int i = 0; i < NB; ++i) v[i] = i * 32 + lane < nc ? mass(i * 32 + lane) : 0.0;
-        double carry = 0.0;
-#pragma unroll 1
         for (int i = 0; i < NB; ++i) {
-            incl[i] = carry + warp_incl_scan(v[i]);
-            carry = __shfl_sync(0xffffffffu, incl[i], 31);
+            const int c = lane * NB + i;
+            v[i] = c < nc ? mass(c) : 0.0;
         }
-        pk.total = carry;
-        if (!(carry > 0.0)) return pk;
-        const double t = double(u) * carry;
+        double sl = 0.0;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) sl += v[i];
+        const double incl = warp_incl_scan(sl);
+        const double total = __shfl_sync(0xffffffffu, incl, 31);
+        pk.total = total;
+        if (!(total > 0.0)) return pk;
+        const double t = double(u) * total;
+        const double ex = __shfl_up_sync(0xffffffffu, incl, 1);
+        double run = lane == 0 ? 0.0 : ex;
+        int cand = -1, lastpos = -1;
+        double cbefore = 0.0, lbefore = 0.0;
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
-            const double prev = __shfl_up_sync(0xffffffffu, incl[i], 1);
-            const double first = i == 0 ? 0.0 : __shfl_sync(0xffffffffu, incl[i == 0 ? 0 : i - 1], 31);
-            const unsigned hit = __ballot_sync(0xffffffffu, incl[i] >= t && v[i] > 0.0);
-            if (hit && pk.chunk < 0) {
-                const int l = __ffs(hit) - 1;
-                pk.chunk = i * 32 + l;
-                pk.before = __shfl_sync(0xffffffffu, lane == 0 ? first : prev, l);
+            const double nr = run + v[i];
+            if (v[i] > 0.0) {
+                if (cand < 0 && nr >= t) {
+                    cand = lane * NB + i;
+                    cbefore = run;
+                }
+                lastpos = lane * NB + i;
+                lbefore = run;
             }
+            run = nr;
+        }
+        unsigned hit = __ballot_sync(0xffffffffu, cand >= 0);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            pk.chunk = __shfl_sync(0xffffffffu, cand, l);
+            pk.before = __shfl_sync(0xffffffffu, cbefore, l);
+        } else {  // rounding left the threshold past the end: the last chunk of positive mass
+            hit = __ballot_sync(0xffffffffu, lastpos >= 0);
+            const int l = 31 - __clz(hit);
+            pk.chunk = __shfl_sync(0xffffffffu, lastpos, l);
+            pk.before = __shfl_sync(0xffffffffu, lbefore, l);
         }
         return pk;
     }
@@ -202,40 +225,36 @@ template <typename WeightFn>
 __device__ __noinline__ int level2(int c0, int nel, float t, WeightFn weight8) {
     const int lane = threadIdx.x & 31;
     constexpr int G = TILE / 8 / 32;
-    float gsum[G];
-    int glast[G];  // last positive token of the group (-1: none)
+    // block k by block k: the group sums of the block, their scan (carried
+    // from the blocks before), and a stop at the first block that reaches t
+    float carry = 0.f, before = 0.f;
+    int found = -1, last = -1;  // last: the last token of positive mass seen
 #pragma unroll 1
     for (int k = 0; k < G; ++k) {
         const int g = k * 32 + lane;
-        gsum[k] = 0.f;
-        glast[k] = -1;
+        float gs = 0.f;
         if (g * 8 < nel) {
             float w[8];
             weight8(g, w);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                gsum[k] = __fadd_rn(gsum[k], w[e]);
-                if (w[e] > 0.f) glast[k] = g * 8 + e;
+                gs = __fadd_rn(gs, w[e]);
+                if (w[e] > 0.f) last = g * 8 + e;
             }
         }
-    }
-    float carry = 0.f;
-    int found = -1;
-    float before = 0.f;
-#pragma unroll 1
-    for (int k = 0; k < G; ++k) {
-        float incl = gsum[k];
+        float incl = gs;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl = __fadd_rn(incl, y);
         }
         incl = __fadd_rn(carry, incl);
-        const unsigned hit = __ballot_sync(0xffffffffu, incl >= t && gsum[k] > 0.f);
-        if (hit && found < 0) {
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= t && gs > 0.f);
+        if (hit) {
             const int l = __ffs(hit) - 1;
             found = k * 32 + l;
-            before = __shfl_sync(0xffffffffu, __fsub_rn(incl, gsum[k]), l);
+            before = __shfl_sync(0xffffffffu, __fsub_rn(incl, gs), l);
+            break;
         }
         carry = __shfl_sync(0xffffffffu, incl, 31);
     }
@@ -258,9 +277,6 @@ __device__ __noinline__ int level2(int c0, int nel, float t, WeightFn weight8) {
         }
         x = __shfl_sync(0xffffffffu, x, found & 31);
     } else {
-        int last = -1;
-#pragma unroll
-        for (int k = 0; k < G; ++k) last = max(last, glast[k]);
         x = warp_max_int(last);
     }
     return c0 + (x < 0 ? 0 : x);
