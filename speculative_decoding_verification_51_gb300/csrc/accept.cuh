@@ -91,24 +91,30 @@ __device__ __forceinline__ AccLoads accept_loads(const Params& P, int b, int n, 
 // max (greedy rows).  With at most 128 chunks a lane's chunks stay in
 // registers: the max first (shuffles), then every chunk rebased onto it once
 // (one ex2 each) and summed (shuffles); longer rows merge pairwise.
-__device__ __forceinline__ void merge_row(const Partial* prow, int C, bool greedy, float kappa,
-                                          float& M, float& Z, int& A) {
+constexpr int MERGE_NPL = 4;  // chunks per lane held in registers (rows of up to 128 chunks)
+
+// This lane's chunk partials of a row of C <= 32 * MERGE_NPL chunks.
+__device__ __forceinline__ void load_row(const Partial* prow, int C, Partial (&q)[MERGE_NPL]) {
     const int lane = threadIdx.x & 31;
-    constexpr int NPL = 4;  // chunks per lane held in registers
-    if (C <= 32 * NPL) {
-        Partial q[NPL];
 #pragma unroll
-        for (int i = 0; i < NPL; ++i) {
-            const int c = lane + 32 * i;
-            if (c < C) {
-                const double2 raw = __ldcg(reinterpret_cast<const double2*>(prow + c));
-                q[i] = *reinterpret_cast<const Partial*>(&raw);
-            } else {
-                q[i].m = -INFINITY;
-                q[i].amax = INT_MAX;
-                q[i].z = 0.0;
-            }
+    for (int i = 0; i < MERGE_NPL; ++i) {
+        const int c = lane + 32 * i;
+        if (c < C) {
+            const double2 raw = __ldcg(reinterpret_cast<const double2*>(prow + c));
+            q[i] = *reinterpret_cast<const Partial*>(&raw);
+        } else {
+            q[i].m = -INFINITY;
+            q[i].amax = INT_MAX;
+            q[i].z = 0.0;
         }
+    }
+}
+
+// merge_row on partials already loaded by load_row.
+__device__ __forceinline__ void merge_loaded(const Partial (&q)[MERGE_NPL], bool greedy, float kappa,
+                                             float& M, float& Z, int& A) {
+    constexpr int NPL = MERGE_NPL;
+    {
         float lm = -INFINITY;
 #pragma unroll
         for (int i = 0; i < NPL; ++i) lm = fmaxf(lm, q[i].m);
@@ -131,6 +137,16 @@ __device__ __forceinline__ void merge_row(const Partial* prow, int C, bool greed
             }
             Z = warp_sum_f(lz);
         }
+    }
+}
+
+__device__ __forceinline__ void merge_row(const Partial* prow, int C, bool greedy, float kappa,
+                                          float& M, float& Z, int& A) {
+    const int lane = threadIdx.x & 31;
+    if (C <= 32 * MERGE_NPL) {
+        Partial q[MERGE_NPL];
+        load_row(prow, C, q);
+        merge_loaded(q, greedy, kappa, M, Z, A);
     } else {  // long vocabularies: pairwise merges over the lane's chunks
         float m = -INFINITY;
         int am = INT_MAX;

@@ -340,7 +340,7 @@ __global__ void k_emit_f32(Params P);
 __global__ void k_emit_bf16(Params P);
 
 __global__ void k_accept_all(Params P);  // one CTA per request, after the row statistics
-constexpr int ACCEPT_WARPS = 4;          // warps of a k_accept_all CTA
+constexpr int ACCEPT_WARPS = 8;          // warps of a k_accept_all CTA
 __global__ void k_tree_walk_f32(Params P);
 __global__ void k_tree_walk_bf16(Params P);
 #ifndef SV_TREE_THREADS

@@ -367,20 +367,32 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
 __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept_all(Params P) {
     griddep_wait();  // the row statistics
     const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (b >= P.B || P.req_flags[b] != 0) return;  // bad requests: k_plan wrote their outputs
+    if (b >= P.B) return;
     __shared__ float s_m[SPEC_MAX_K + 1], s_z[SPEC_MAX_K + 1];
     __shared__ int s_a[SPEC_MAX_K + 1];
+    // Loads that need nothing loaded first go out together with num_draft
+    // and temperature: each warp's first row of partials, and warp 0's draft
+    // tokens, gathers and Philox blocks for every row the request may have
+    // (rows past num_draft are never used).
+    const Partial* pb = P.part + (size_t)b * P.K1 * P.C;
+    Partial q0[MERGE_NPL];
+    const bool pre = P.C <= 32 * MERGE_NPL && warp < P.K1;
+    if (pre) load_row(pb + (size_t)warp * P.C, P.C, q0);
+    AccLoads L;
+    if (warp == 0) L = accept_loads(P, b, P.K, false, 0, P.K);
+    const int flags = P.req_flags[b];
     const int n = P.num_draft[b];
     const float T = P.temp[b];
+    if (flags != 0) return;  // bad requests: k_plan wrote their outputs
     const bool greedy = (T == 0.f);
     const float kappa = greedy ? 0.f : kappa_of(T);
-    AccLoads L;
-    if (warp == 0) L = accept_loads(P, b, n, greedy, 0, n);
-    const Partial* pb = P.part + (size_t)b * P.K1 * P.C;
     for (int j = warp; j <= n; j += ACCEPT_WARPS) {
         float M, Z;
         int A;
-        merge_row(pb + (size_t)j * P.C, P.C, greedy, kappa, M, Z, A);
+        if (j == warp && pre)
+            merge_loaded(q0, greedy, kappa, M, Z, A);
+        else
+            merge_row(pb + (size_t)j * P.C, P.C, greedy, kappa, M, Z, A);
         if (lane == 0) {
             s_m[j] = M;
             s_z[j] = Z;
