@@ -451,39 +451,36 @@ __device__ __forceinline__ void tree_walk_body(const Params& P) {
                         chain8(p, s_ch, kk, s_qrows, y0, w);
                     }
                 };
-                float gsum[GROUPS];
-                int glast[GROUPS];
+                // block k by block k: group sums, their scan carried from the
+                // blocks before, and a stop at the first block reaching tloc
+                float carry_f = 0.f, bef = 0.f;
+                int found = -1, glast_all = -1;
 #pragma unroll 1
                 for (int k = 0; k < GROUPS; ++k) {
                     const int g = k * 32 + lane;
-                    gsum[k] = 0.f;
-                    glast[k] = -1;
+                    float gs = 0.f;
                     if (g * 8 < nel) {
                         float w[8];
                         weight8(g, w);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
-                            gsum[k] = __fadd_rn(gsum[k], w[e]);
-                            if (w[e] > 0.f) glast[k] = g * 8 + e;
+                            gs = __fadd_rn(gs, w[e]);
+                            if (w[e] > 0.f) glast_all = g * 8 + e;
                         }
                     }
-                }
-                float carry_f = 0.f, bef = 0.f;
-                int found = -1;
-#pragma unroll 1
-                for (int k = 0; k < GROUPS; ++k) {
-                    float incl = gsum[k];
+                    float incl = gs;
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) {
                         const float y = __shfl_up_sync(0xffffffffu, incl, o);
                         if (lane >= o) incl = __fadd_rn(incl, y);
                     }
                     incl = __fadd_rn(carry_f, incl);
-                    const unsigned hit = __ballot_sync(0xffffffffu, incl >= tloc && gsum[k] > 0.f);
-                    if (hit && found < 0) {
+                    const unsigned hit = __ballot_sync(0xffffffffu, incl >= tloc && gs > 0.f);
+                    if (hit) {
                         const int l = __ffs(hit) - 1;
                         found = k * 32 + l;
-                        bef = __shfl_sync(0xffffffffu, __fsub_rn(incl, gsum[k]), l);
+                        bef = __shfl_sync(0xffffffffu, __fsub_rn(incl, gs), l);
+                        break;
                     }
                     carry_f = __shfl_sync(0xffffffffu, incl, 31);
                 }
@@ -506,10 +503,7 @@ __device__ __forceinline__ void tree_walk_body(const Params& P) {
                     }
                     xl = __shfl_sync(0xffffffffu, xl, found & 31);
                 } else {
-                    int last = -1;
-#pragma unroll
-                    for (int k = 0; k < GROUPS; ++k) last = max(last, glast[k]);
-                    xl = warp_max_int(last);
+                    xl = warp_max_int(glast_all);
                 }
                 x = c0 + (xl < 0 ? 0 : xl);
             }
