@@ -26,9 +26,13 @@ DeviceInfo g_dev[kMaxDevices];
 constexpr size_t stats_smem(int dtype) {
     return size_t(STATS_WARPS) * STATS_STAGES * TILE * (dtype == SPEC_BF16 ? 2 : 4);
 }
-// two stages per warp of (logits chunk + draft-probability chunk)
+// k_sample: two stages per warp pair of (logits chunk + draft-probability chunk)
 constexpr size_t sample_smem(int dtype) {
-    return size_t(SAMPLE_WARPS) * 2 * TILE * ((dtype == SPEC_BF16 ? 2 : 4) + 4);
+    return size_t(SAMPLE_PAIRS) * 2 * TILE * ((dtype == SPEC_BF16 ? 2 : 4) + 4);
+}
+// k_emit: one such stage per warp
+constexpr size_t emit_smem(int dtype) {
+    return size_t(SAMPLE_WARPS) * TILE * ((dtype == SPEC_BF16 ? 2 : 4) + 4);
 }
 
 // Per-device launch facts, computed once per device (thread-safe).
@@ -49,9 +53,9 @@ spec_status device_info(DeviceInfo& out) {
             cudaFuncSetAttribute(k_sample_f32, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(sample_smem(SPEC_F32))) != cudaSuccess ||
             cudaFuncSetAttribute(k_emit_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(sample_smem(SPEC_BF16) / 2)) != cudaSuccess ||
+                                 int(emit_smem(SPEC_BF16))) != cudaSuccess ||
             cudaFuncSetAttribute(k_emit_f32, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(sample_smem(SPEC_F32) / 2)) != cudaSuccess)
+                                 int(emit_smem(SPEC_F32))) != cudaSuccess)
             return SPEC_ERR_CUDA;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.stats_blocks_bf16,
                                                           k_row_stats_bf16, STATS_WARPS * 32,
@@ -60,10 +64,10 @@ spec_status device_info(DeviceInfo& out) {
                                                           k_row_stats_f32, STATS_WARPS * 32,
                                                           stats_smem(SPEC_F32)) != cudaSuccess ||
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sample_blocks_bf16, k_sample_bf16,
-                                                          SAMPLE_WARPS * 32,
+                                                          SAMPLE_PAIRS * 64,
                                                           sample_smem(SPEC_BF16)) != cudaSuccess ||
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sample_blocks_f32, k_sample_f32,
-                                                          SAMPLE_WARPS * 32,
+                                                          SAMPLE_PAIRS * 64,
                                                           sample_smem(SPEC_F32)) != cudaSuccess)
             return SPEC_ERR_CUDA;
         d.stats_blocks_bf16 = d.stats_blocks_bf16 < 1 ? 1 : d.stats_blocks_bf16;
@@ -187,7 +191,7 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     const long long need1 = (max_tiles + STATS_WARPS - 1) / STATS_WARPS;
     if (g1 > need1) g1 = need1;
     long long g3 = (long long)dev.sms * (bf16 ? dev.sample_blocks_bf16 : dev.sample_blocks_f32);
-    const long long need3 = ((long long)B * P.C + SAMPLE_WARPS - 1) / SAMPLE_WARPS;
+    const long long need3 = ((long long)B * P.C + SAMPLE_PAIRS - 1) / SAMPLE_PAIRS;
     if (g3 > need3) g3 = need3;
     const unsigned g4 = unsigned((B + SAMPLE_WARPS - 1) / SAMPLE_WARPS);  // a warp per draw
 
@@ -226,12 +230,12 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
         e = launch(k_accept_all, unsigned(B), ACCEPT_WARPS * 32, 0, st, true, P);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess)
-        e = launch(bf16 ? k_sample_bf16 : k_sample_f32, unsigned(g3), SAMPLE_WARPS * 32,
+        e = launch(bf16 ? k_sample_bf16 : k_sample_f32, unsigned(g3), SAMPLE_PAIRS * 64,
                    sample_smem(logits_dtype), st, true, P);
     if (e == cudaSuccess) e = mark(4);
     if (e == cudaSuccess)
         e = launch(bf16 ? k_emit_bf16 : k_emit_f32, g4, SAMPLE_WARPS * 32,
-                   sample_smem(logits_dtype) / 2, st, true, P);
+                   emit_smem(logits_dtype), st, true, P);
     if (e == cudaSuccess) e = mark(5);
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

@@ -20,9 +20,9 @@
 //            its last token of positive mass is.
 // Every unit of work belongs to one warp and warps never wait for each other.
 // k_sample: a residual unit is one chunk of (logits row, draft row) whose mass
-// is stored; the warp copies the chunk into shared memory with two 1-D bulk
-// copies (cp.async.bulk, mbarrier completion) while the previous unit is being
-// reduced (two stages per warp).  k_emit (the next kernel, once the memory
+// is stored; a pair of warps copies the chunk into shared memory with two 1-D
+// bulk copies (cp.async.bulk, mbarrier completion) while the previous unit is
+// being reduced (two stages per pair), each warp reducing half its groups.  k_emit (the next kernel, once the memory
 // system is free of the streaming traffic): one warp per draw, residual or
 // bonus, runs both levels.
 #include <cfloat>
@@ -96,12 +96,15 @@ struct WarpStages {
         }
         inflight |= 1u << s;
     }
-    // whole warp: wait for stage s (bounded); false if the wait gave up
+    // whole warp: wait for stage s (bounded); false if the wait gave up, and
+    // then the copy still counts as in flight
     __device__ __forceinline__ bool wait(int s) {
-        const bool ok = mbar_wait_bounded(bars + s, (phase >> s) & 1u);
-        phase ^= 1u << s;
-        inflight &= ~(1u << s);
-        return __all_sync(0xffffffffu, ok);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bars + s, (phase >> s) & 1u));
+        if (ok) {
+            phase ^= 1u << s;
+            inflight &= ~(1u << s);
+        }
+        return ok;
     }
 };
 
@@ -320,37 +323,74 @@ __device__ void emit_from_p(const Params& P, const ReqRec& rec, int mode, WarpSt
     write_emit(P, rec, x, mode, pk.total);
 }
 
-// Residual mass of a staged chunk of nel tokens (coalesced 8-token groups,
-// pairwise float32 sums, warp shuffle sum).
-template <int DT>
-__device__ __forceinline__ float staged_residual_sum(const uint8_t* st, int nel, const ReqRec& rec) {
+// One warp's share of the residual mass of a staged chunk of nel tokens.  The
+// chunk's 8-token groups are k * 32 + l (lane l, k = 0..7, coalesced); warp
+// `odd` of the pair takes k = odd, odd + 2, odd + 4, odd + 6, sums each
+// group's 8 weights pairwise in float32, then (k, k + 4) pairs and the two
+// pair sums.  The even warp's value plus the odd warp's, summed over the lanes,
+// is the pairwise sum of the lane's 8 groups.  FIN: the row offset is finite
+// (the weight exponent is one FFMA, as weight_arg computes it then).
+template <int DT, bool FIN>
+__device__ __forceinline__ float staged_residual_half(const uint8_t* st, int nel,
+                                                      const ReqRec& rec, int odd) {
     const int lane = threadIdx.x & 31;
     const float invZ = float(1.0 / rec.Z);
     const float cm = offset_of(rec.m, rec.kappa);
-    constexpr int G = TILE / 8 / 32;
-    float gs[G];
+    float gs[4];
 #pragma unroll
-    for (int k = 0; k < G; ++k) {
-        const int g = k * 32 + lane;
-        gs[k] = 0.f;
+    for (int t = 0; t < 4; ++t) {
+        const int g = (2 * t + odd) * 32 + lane;
+        gs[t] = 0.f;
         if (g * 8 < nel) {
             float l[8], q[8];
             smem_logits8<DT>(st, g, l);
             smem_q8(st + Stage<DT>::LB, g, q);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) l[e] = resid(l[e], q[e], rec.m, cm, rec.kappa, invZ);
+            for (int e = 0; e < 8; ++e) {
+                const float arg = FIN ? fmaf(l[e], rec.kappa, -cm)
+                                      : __fmul_rn(__fsub_rn(l[e], rec.m), rec.kappa);
+                const float p = __fmul_rn(ex2_approx(arg), invZ);
+                l[e] = fmaxf(__fsub_rn(p, q[e]), 0.f);
+            }
 #pragma unroll
             for (int h = 4; h; h >>= 1)
 #pragma unroll
                 for (int e = 0; e < h; ++e) l[e] = __fadd_rn(l[e], l[e + h]);
-            gs[k] = l[0];
+            gs[t] = l[0];
         }
     }
-#pragma unroll
-    for (int h = G / 2; h; h >>= 1)
-#pragma unroll
-        for (int k = 0; k < h; ++k) gs[k] = __fadd_rn(gs[k], gs[k + h]);
-    return warp_sum_f(gs[0]);
+    return __fadd_rn(__fadd_rn(gs[0], gs[2]), __fadd_rn(gs[1], gs[3]));
+}
+
+// bar.red.and over the 64 threads of warp pair `pair` (named barrier 1 + pair):
+// true iff every thread's `ok` is; also orders the pair's shared-memory accesses.
+// The barrier number is a literal in each case so that only the barriers in use
+// are reserved.
+template <int ID>
+__device__ __forceinline__ bool bar_red_and64(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "barrier.red.and.pred po, %2, 64, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(uint32_t(ok)), "n"(ID)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ bool pair_and(int pair, bool ok) {
+    static_assert(SAMPLE_PAIRS <= 8, "one named barrier per pair");
+    switch (pair) {
+        case 0: return bar_red_and64<1>(ok);
+        case 1: return bar_red_and64<2>(ok);
+        case 2: return bar_red_and64<3>(ok);
+        case 3: return bar_red_and64<4>(ok);
+        case 4: return bar_red_and64<5>(ok);
+        case 5: return bar_red_and64<6>(ok);
+        case 6: return bar_red_and64<7>(ok);
+        default: return bar_red_and64<8>(ok);
+    }
 }
 
 // Level 1 and 2 of the residual of queued request i, by the warp that
@@ -419,25 +459,40 @@ __device__ __forceinline__ void finish_stages(const Params& P, WarpStages& ws) {
     }
 }
 
-// k_sample: the residual chunk masses of every queued request, one warp per
-// 2048-token chunk.  Each warp takes an equal contiguous range of the units
-// (queue entry i, chunk c) in order and keeps two staging buffers: the next
-// chunk's bulk copies are in flight while the current one is reduced.  A pure
-// streaming pass: the draws themselves are made by k_emit.
+// k_sample: the residual chunk masses of every queued request.  Each pair of
+// warps takes an equal contiguous range of the units (queue entry i, chunk c)
+// in order and keeps two staging buffers: the next chunk's bulk copies (issued
+// by the even warp) are in flight while both warps reduce the current one.
+// Sharing each chunk between two warps doubles the warps per SM for the same
+// shared memory.  A pure streaming pass: the draws themselves are made by
+// k_emit.
 template <int DT>
 __device__ __forceinline__ void sample_body(const Params& P) {
     using ST = Stage<DT>;
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bars[SAMPLE_WARPS * 2];
-    WarpStages ws = make_stages<DT>(smem, bars, 2);
+    __shared__ __align__(8) uint64_t bars[SAMPLE_PAIRS * 2];
+    __shared__ float xch[SAMPLE_PAIRS][2][32];  // the odd warp's lane sums, per stage
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pair = warp >> 1, odd = warp & 1;
+    WarpStages ws;
+    ws.base = smem + size_t(pair) * 2 * ST::BYTES;
+    ws.bars = bars + pair * 2;
+    ws.stage_bytes = ST::BYTES;
+    ws.phase = 0;
+    ws.inflight = 0;
+    ws.broken = false;
+    if (threadIdx.x < SAMPLE_PAIRS * 2) {
+        mbar_init(bars + threadIdx.x, 1);
+        fence_mbarrier_init();
+    }
+    __syncthreads();
     griddep_launch_dependents();
     griddep_wait();  // decisions and queues of the acceptance step
-    const int lane = threadIdx.x & 31;
-    const long long W = (long long)gridDim.x * SAMPLE_WARPS;
-    const long long wid = (long long)blockIdx.x * SAMPLE_WARPS + (threadIdx.x >> 5);
+    const long long W = (long long)gridDim.x * SAMPLE_PAIRS;
+    const long long pid = (long long)blockIdx.x * SAMPLE_PAIRS + pair;
     const long long VT = (long long)P.hdr[HDR_NRES] * P.C;
-    const long long r0 = VT * wid / W, r1 = VT * (wid + 1) / W;
-    auto issue_res = [&](long long v, const ReqRec& r, int s) {
+    const long long r0 = VT * pid / W, r1 = VT * (pid + 1) / W;
+    auto issue_res = [&](long long v, const ReqRec& r, int s) {  // even warp only
         const int c = int(v % P.C);
         const int c0 = c * TILE, nel = min(TILE, P.V - c0);
         const char* l = reinterpret_cast<const char*>(P.logits) +
@@ -445,31 +500,39 @@ __device__ __forceinline__ void sample_body(const Params& P) {
         const float* q = P.probs + ((size_t)r.b * P.K + r.erow) * P.V + c0;
         ws.issue(s, l, uint32_t(nel) * ST::ESZ, q, uint32_t(nel) * 4u, ST::LB);
     };
-    if (r0 < r1) {
+    if (r0 < r1) {  // uniform over the pair
         int s = 0;
         ReqRec cur = P.res_rec[r0 / P.C];
-        issue_res(r0, cur, s);
+        if (!odd) issue_res(r0, cur, s);
         for (long long v = r0; v < r1; ++v) {
             const long long i = v / P.C;
             const int c = int(v - i * P.C);
             const long long next = v + 1;
             ReqRec nxt = cur;
-            if (next < r1) {  // stage the next chunk while this one is reduced
+            if (next < r1) {  // stage s ^ 1 was released by both warps at the last pair barrier
                 if (next / P.C != i) nxt = P.res_rec[next / P.C];
-                issue_res(next, nxt, s ^ 1);
+                if (!odd) issue_res(next, nxt, s ^ 1);
             }
-            if (!ws.wait(s)) {
+            const bool ok = ws.wait(s);
+            // a stage that did not land is still read (in bounds) but its sum is dropped
+            const int nel = min(TILE, P.V - c * TILE);
+            const float part = isfinite(offset_of(cur.m, cur.kappa))
+                                   ? staged_residual_half<DT, true>(ws.buf(s), nel, cur, odd)
+                                   : staged_residual_half<DT, false>(ws.buf(s), nel, cur, odd);
+            if (odd) xch[pair][s][lane] = part;
+            if (!pair_and(pair, ok)) {  // the same decision in both warps
                 ws.broken = true;
                 break;
             }
-            const float sum = staged_residual_sum<DT>(ws.buf(s), min(TILE, P.V - c * TILE), cur);
-            __syncwarp();  // stage s has been read
-            if (lane == 0) P.rsum[(size_t)i * P.C + c] = sum;
+            if (!odd) {
+                const float sum = warp_sum_f(__fadd_rn(part, xch[pair][s][lane]));
+                if (lane == 0) P.rsum[(size_t)i * P.C + c] = sum;
+            }
             cur = nxt;
             s ^= 1;
         }
     }
-    finish_stages(P, ws);
+    finish_stages(P, ws);  // the even warp waits for its copies still in flight
 }
 
 // k_emit: one warp per draw once every residual mass exists: the residual
@@ -497,10 +560,10 @@ __device__ __forceinline__ void emit_body(const Params& P) {
     finish_stages(P, ws);
 }
 
-__global__ void __launch_bounds__(SAMPLE_WARPS * 32) k_sample_f32(Params P) {
+__global__ void __launch_bounds__(SAMPLE_PAIRS * 64) k_sample_f32(Params P) {
     sample_body<SPEC_F32>(P);
 }
-__global__ void __launch_bounds__(SAMPLE_WARPS * 32) k_sample_bf16(Params P) {
+__global__ void __launch_bounds__(SAMPLE_PAIRS * 64) k_sample_bf16(Params P) {
     sample_body<SPEC_BF16>(P);
 }
 __global__ void __launch_bounds__(SAMPLE_WARPS * 32) k_emit_f32(Params P) { emit_body<SPEC_F32>(P); }
