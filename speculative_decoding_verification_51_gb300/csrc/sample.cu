@@ -225,7 +225,7 @@ __device__ __forceinline__ Pick pick_chunk(int nc, float u, MassFn mass) {
 // are visited in token order g = 32 k + lane; returns the first token whose
 // running sum reaches t, or the chunk's last token of positive mass.
 template <typename WeightFn>
-__device__ __noinline__ int level2(int c0, int nel, float t, WeightFn weight8) {
+__device__ __forceinline__ int level2(int c0, int nel, float t, WeightFn weight8) {
     const int lane = threadIdx.x & 31;
     constexpr int G = TILE / 8 / 32;
     // block k by block k: the group sums of the block, their scan (carried
@@ -288,7 +288,8 @@ __device__ __noinline__ int level2(int c0, int nel, float t, WeightFn weight8) {
 // Draw from p of row rec.erow using the row-stat partials (bonus token, or the
 // residual when it has no mass).  Level 2 stages the chunk in stage s.
 template <int DT>
-__device__ void emit_from_p(const Params& P, const ReqRec& rec, int mode, WarpStages& ws, int s) {
+__device__ __forceinline__ void emit_from_p(const Params& P, const ReqRec& rec, int mode,
+                                            WarpStages& ws, int s) {
     const Partial* part = P.part + ((size_t)rec.b * P.K1 + rec.erow) * P.C;
     const float m = rec.m, kappa = rec.kappa;
     const Pick pk = pick_chunk(P.C, rec.u2, [&](int c) -> double {
@@ -396,7 +397,8 @@ __device__ __forceinline__ bool pair_and(int pair, bool ok) {
 // Level 1 and 2 of the residual of queued request i, by the warp that
 // completed its last chunk sum.  Level 2 stages the chunk in stage s.
 template <int DT>
-__device__ void emit_residual(const Params& P, const ReqRec& rec, int i, WarpStages& ws, int s) {
+__device__ __forceinline__ void emit_residual(const Params& P, const ReqRec& rec, int i,
+                                              WarpStages& ws, int s) {
     const float* rs = P.rsum + (size_t)i * P.C;
     const Pick pk = pick_chunk(P.C, rec.u2, [&](int c) -> double { return double(__ldcg(rs + c)); });
     if (pk.chunk < 0) {  // residual without mass: draw from p instead
@@ -549,11 +551,12 @@ __device__ __forceinline__ void emit_body(const Params& P) {
     const int n_res = P.hdr[HDR_NRES], n_bonus = P.hdr[HDR_NBONUS];
     for (long long k = (long long)blockIdx.x * SAMPLE_WARPS + (threadIdx.x >> 5);
          k < n_res + n_bonus && !ws.broken; k += W) {
-        if (k < n_res)
-            emit_residual<DT>(P, P.res_rec[k], int(k), ws, 0);
-        else
-            {
-            const ReqRec& r = P.bonus_rec[k - n_res];
+        // the record is copied to registers: every step of the draw reads it
+        if (k < n_res) {
+            const ReqRec r = P.res_rec[k];
+            emit_residual<DT>(P, r, int(k), ws, 0);
+        } else {
+            const ReqRec r = P.bonus_rec[k - n_res];
             emit_from_p<DT>(P, r, r.mode, ws, 0);
         }
     }
