@@ -32,7 +32,7 @@ constexpr size_t sample_smem(int dtype) {
 }
 // k_emit: one such stage per warp
 constexpr size_t emit_smem(int dtype) {
-    return size_t(SAMPLE_WARPS) * TILE * ((dtype == SPEC_BF16 ? 2 : 4) + 4);
+    return size_t(EMIT_WARPS) * TILE * ((dtype == SPEC_BF16 ? 2 : 4) + 4);
 }
 
 // Per-device launch facts, computed once per device (thread-safe).
@@ -193,7 +193,8 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     long long g3 = (long long)dev.sms * (bf16 ? dev.sample_blocks_bf16 : dev.sample_blocks_f32);
     const long long need3 = ((long long)B * P.C + SAMPLE_PAIRS - 1) / SAMPLE_PAIRS;
     if (g3 > need3) g3 = need3;
-    const unsigned g4 = unsigned((B + SAMPLE_WARPS - 1) / SAMPLE_WARPS);  // a warp per draw
+    // k_emit: a warp per slot of the residual and of the bonus queue
+    const unsigned g4 = unsigned((2LL * B + EMIT_WARPS - 1) / EMIT_WARPS);
 
     // events (profiling only) are recorded before each kernel and after the last
     auto mark = [&](int i) { return events ? cudaEventRecord(events[i], st) : cudaSuccess; };
@@ -234,7 +235,7 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
                    sample_smem(logits_dtype), st, true, P);
     if (e == cudaSuccess) e = mark(4);
     if (e == cudaSuccess)
-        e = launch(bf16 ? k_emit_bf16 : k_emit_f32, g4, SAMPLE_WARPS * 32,
+        e = launch(bf16 ? k_emit_bf16 : k_emit_f32, g4, EMIT_WARPS * 32,
                    emit_smem(logits_dtype), st, true, P);
     if (e == cudaSuccess) e = mark(5);
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

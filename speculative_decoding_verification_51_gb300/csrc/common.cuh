@@ -37,8 +37,8 @@ namespace sv {
 #ifndef SV_STATS_STAGES
 #define SV_STATS_STAGES 3
 #endif
-#ifndef SV_SAMPLE_WARPS
-#define SV_SAMPLE_WARPS 4
+#ifndef SV_EMIT_WARPS
+#define SV_EMIT_WARPS 1
 #endif
 #ifndef SV_SAMPLE_PAIRS
 #define SV_SAMPLE_PAIRS 4
@@ -47,7 +47,7 @@ namespace sv {
 constexpr int TILE = 2048;                    // tokens per row-stat chunk (one warp tile)
 constexpr int STATS_WARPS = SV_STATS_WARPS;   // warps per k_row_stats CTA
 constexpr int STATS_STAGES = SV_STATS_STAGES; // bulk-copy stages per warp
-constexpr int SAMPLE_WARPS = SV_SAMPLE_WARPS;  // warps per k_emit CTA (1 staging buffer each)
+constexpr int EMIT_WARPS = SV_EMIT_WARPS;      // warps per k_emit CTA (1 staging buffer each)
 constexpr int SAMPLE_PAIRS = SV_SAMPLE_PAIRS;  // warp pairs per k_sample CTA (2 shared staging buffers each)
 constexpr int PLAN_THREADS = 1024;
 

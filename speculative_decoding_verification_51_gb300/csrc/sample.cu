@@ -140,24 +140,31 @@ __device__ __forceinline__ double warp_incl_scan(double x) {
 // Level 1 over nc chunk masses mass(c) in chunk order, by one warp: S = the
 // total; the chosen chunk is the first of positive mass whose prefix reaches
 // u * S (the last of positive mass if rounding leaves u * S beyond every
-// prefix).  Up to 128 chunks are loaded at once (one round trip) and summed
-// with one warp scan; beyond, block by block.
+// prefix).  Up to PICK_NB * 32 chunks are loaded at once (one round trip) and
+// summed with one warp scan; beyond, block by block.
+constexpr int PICK_NB = 4;
+
+// Lane l holds chunks PICK_NB*l .. PICK_NB*l + PICK_NB - 1 (0 past nc), so
+// chunk order runs lane by lane.  For nc <= PICK_NB * 32.
 template <typename MassFn>
-__device__ __forceinline__ Pick pick_chunk(int nc, float u, MassFn mass) {
+__device__ __forceinline__ void load_masses(int nc, MassFn mass, double (&v)[PICK_NB]) {
     const int lane = threadIdx.x & 31;
-    constexpr int NB = 4;
+#pragma unroll
+    for (int i = 0; i < PICK_NB; ++i) {
+        const int c = lane * PICK_NB + i;
+        v[i] = c < nc ? mass(c) : 0.0;
+    }
+}
+
+// The pick over masses held as load_masses holds them: one warp scan of the
+// lane sums, then a walk within the lane.
+__device__ __forceinline__ Pick pick_loaded(float u, const double (&v)[PICK_NB]) {
+    const int lane = threadIdx.x & 31;
+    constexpr int NB = PICK_NB;
     Pick pk;
     pk.chunk = -1;
     pk.before = 0.0;
-    if (nc <= NB * 32) {
-        // lane l holds chunks NB*l .. NB*l + NB - 1, so chunk order runs lane
-        // by lane: one warp scan of the lane sums, then a walk within the lane
-        double v[NB];
-#pragma unroll
-        for (int i = 0; i < NB; ++i) {
-            const int c = lane * NB + i;
-            v[i] = c < nc ? mass(c) : 0.0;
-        }
+    {
         double sl = 0.0;
 #pragma unroll
         for (int i = 0; i < NB; ++i) sl += v[i];
@@ -196,6 +203,19 @@ __device__ __forceinline__ Pick pick_chunk(int nc, float u, MassFn mass) {
         }
         return pk;
     }
+}
+
+template <typename MassFn>
+__device__ __forceinline__ Pick pick_chunk(int nc, float u, MassFn mass) {
+    const int lane = threadIdx.x & 31;
+    if (nc <= PICK_NB * 32) {
+        double v[PICK_NB];
+        load_masses(nc, mass, v);
+        return pick_loaded(u, v);
+    }
+    Pick pk;
+    pk.chunk = -1;
+    pk.before = 0.0;
     double carry = 0.0;
     for (int c0 = 0; c0 < nc; c0 += 32)
         carry = carry + __shfl_sync(0xffffffffu,
@@ -394,13 +414,17 @@ __device__ __forceinline__ bool pair_and(int pair, bool ok) {
     }
 }
 
-// Level 1 and 2 of the residual of queued request i, by the warp that
-// completed its last chunk sum.  Level 2 stages the chunk in stage s.
+// Level 1 and 2 of the residual of queued request i.  pre: the chunk masses
+// as load_masses holds them, loaded by the caller when C <= PICK_NB * 32.
+// Level 2 stages the chunk in stage s.
 template <int DT>
 __device__ __forceinline__ void emit_residual(const Params& P, const ReqRec& rec, int i,
-                                              WarpStages& ws, int s) {
+                                              const double (&pre)[PICK_NB], WarpStages& ws,
+                                              int s) {
     const float* rs = P.rsum + (size_t)i * P.C;
-    const Pick pk = pick_chunk(P.C, rec.u2, [&](int c) -> double { return double(__ldcg(rs + c)); });
+    const Pick pk = P.C <= PICK_NB * 32
+                        ? pick_loaded(rec.u2, pre)
+                        : pick_chunk(P.C, rec.u2, [&](int c) -> double { return double(__ldcg(rs + c)); });
     if (pk.chunk < 0) {  // residual without mass: draw from p instead
         emit_from_p<DT>(P, rec, MODE_FALLBACK, ws, s);
         return;
@@ -537,29 +561,37 @@ __device__ __forceinline__ void sample_body(const Params& P) {
     finish_stages(P, ws);  // the even warp waits for its copies still in flight
 }
 
-// k_emit: one warp per draw once every residual mass exists: the residual
-// draws of the rejecting requests, then the bonus draws of the requests whose
-// drafts were all accepted.
+// k_emit: one warp per queue slot once every residual mass exists: even
+// warps take the residual queue's slots, odd warps the bonus queue's (draws
+// from p), so that the filled slots of both queues spread over the SMs (the
+// draws' float64 steps share an SM's narrow FP64 pipe).  A warp loads its
+// slot's count, record and (residual) chunk masses together, all in bounds
+// whether or not the slot is filled, and leaves if it is not: no load of the
+// draw waits for another.
 template <int DT>
 __device__ __forceinline__ void emit_body(const Params& P) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bars[SAMPLE_WARPS * 2];
+    __shared__ __align__(8) uint64_t bars[EMIT_WARPS * 2];
     WarpStages ws = make_stages<DT>(smem, bars, 1);
     griddep_launch_dependents();
     griddep_wait();  // chunk masses of k_sample
-    const long long W = (long long)gridDim.x * SAMPLE_WARPS;
-    const int n_res = P.hdr[HDR_NRES], n_bonus = P.hdr[HDR_NBONUS];
-    for (long long k = (long long)blockIdx.x * SAMPLE_WARPS + (threadIdx.x >> 5);
-         k < n_res + n_bonus && !ws.broken; k += W) {
-        // the record is copied to registers: every step of the draw reads it
-        if (k < n_res) {
-            const ReqRec r = P.res_rec[k];
-            emit_residual<DT>(P, r, int(k), ws, 0);
-        } else {
-            const ReqRec r = P.bonus_rec[k - n_res];
-            emit_from_p<DT>(P, r, r.mode, ws, 0);
-        }
+    const long long w = (long long)blockIdx.x * EMIT_WARPS + (threadIdx.x >> 5);
+    const bool res = (w & 1) == 0;
+    const int slot = int(w >> 1);
+    if (slot >= P.B) return;  // grid rounding (warp-uniform)
+    const int count = P.hdr[res ? HDR_NRES : HDR_NBONUS];
+    // the record is copied to registers: every step of the draw reads it
+    const ReqRec r = res ? P.res_rec[slot] : P.bonus_rec[slot];
+    double pre[PICK_NB];
+    if (res && P.C <= PICK_NB * 32) {
+        const float* rs = P.rsum + (size_t)slot * P.C;
+        load_masses(P.C, [&](int c) -> double { return double(__ldcg(rs + c)); }, pre);
     }
+    if (slot >= count) return;
+    if (res)
+        emit_residual<DT>(P, r, slot, pre, ws, 0);
+    else
+        emit_from_p<DT>(P, r, r.mode, ws, 0);
     finish_stages(P, ws);
 }
 
@@ -569,8 +601,8 @@ __global__ void __launch_bounds__(SAMPLE_PAIRS * 64) k_sample_f32(Params P) {
 __global__ void __launch_bounds__(SAMPLE_PAIRS * 64) k_sample_bf16(Params P) {
     sample_body<SPEC_BF16>(P);
 }
-__global__ void __launch_bounds__(SAMPLE_WARPS * 32) k_emit_f32(Params P) { emit_body<SPEC_F32>(P); }
-__global__ void __launch_bounds__(SAMPLE_WARPS * 32) k_emit_bf16(Params P) { emit_body<SPEC_BF16>(P); }
+__global__ void __launch_bounds__(EMIT_WARPS * 32) k_emit_f32(Params P) { emit_body<SPEC_F32>(P); }
+__global__ void __launch_bounds__(EMIT_WARPS * 32) k_emit_bf16(Params P) { emit_body<SPEC_BF16>(P); }
 
 
 }  // namespace sv
