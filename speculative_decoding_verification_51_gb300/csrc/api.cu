@@ -26,9 +26,9 @@ DeviceInfo g_dev[kMaxDevices];
 constexpr size_t stats_smem(int dtype) {
     return size_t(STATS_WARPS) * STATS_STAGES * TILE * (dtype == SPEC_BF16 ? 2 : 4);
 }
-// k_sample: two stages per warp pair of (logits chunk + draft-probability chunk)
+// k_sample: SAMPLE_STAGES stages per warp pair of (logits chunk + draft-probability chunk)
 constexpr size_t sample_smem(int dtype) {
-    return size_t(SAMPLE_PAIRS) * 2 * TILE * ((dtype == SPEC_BF16 ? 2 : 4) + 4);
+    return size_t(SAMPLE_PAIRS) * SAMPLE_STAGES * TILE * ((dtype == SPEC_BF16 ? 2 : 4) + 4);
 }
 // k_emit: one such stage per warp
 constexpr size_t emit_smem(int dtype) {

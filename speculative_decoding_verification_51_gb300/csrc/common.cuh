@@ -43,12 +43,17 @@ namespace sv {
 #ifndef SV_SAMPLE_PAIRS
 #define SV_SAMPLE_PAIRS 4
 #endif
+#ifndef SV_SAMPLE_STAGES
+#define SV_SAMPLE_STAGES 2
+#endif
 
 constexpr int TILE = 2048;                    // tokens per row-stat chunk (one warp tile)
 constexpr int STATS_WARPS = SV_STATS_WARPS;   // warps per k_row_stats CTA
 constexpr int STATS_STAGES = SV_STATS_STAGES; // bulk-copy stages per warp
 constexpr int EMIT_WARPS = SV_EMIT_WARPS;      // warps per k_emit CTA (1 staging buffer each)
-constexpr int SAMPLE_PAIRS = SV_SAMPLE_PAIRS;  // warp pairs per k_sample CTA (2 shared staging buffers each)
+constexpr int SAMPLE_PAIRS = SV_SAMPLE_PAIRS;    // warp pairs per k_sample CTA
+constexpr int SAMPLE_STAGES = SV_SAMPLE_STAGES;  // staging buffers per k_sample warp pair
+static_assert(SAMPLE_STAGES >= 2 && SAMPLE_PAIRS * SAMPLE_STAGES <= 32, "k_sample staging");
 constexpr int PLAN_THREADS = 1024;
 
 // HDR_ROUND + r: rows of early-exit round r (r >= 1), listed at rowlist + r * B

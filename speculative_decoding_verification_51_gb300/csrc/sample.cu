@@ -487,60 +487,65 @@ __device__ __forceinline__ void finish_stages(const Params& P, WarpStages& ws) {
 
 // k_sample: the residual chunk masses of every queued request.  Each pair of
 // warps takes an equal contiguous range of the units (queue entry i, chunk c)
-// in order and keeps two staging buffers: the next chunk's bulk copies (issued
-// by the even warp) are in flight while both warps reduce the current one.
-// Sharing each chunk between two warps doubles the warps per SM for the same
-// shared memory.  A pure streaming pass: the draws themselves are made by
-// k_emit.
+// in order and keeps SAMPLE_STAGES staging buffers: the bulk copies of the
+// next SAMPLE_STAGES - 1 chunks (issued by the even warp) are in flight while
+// both warps reduce the current one.  Sharing each chunk between two warps
+// doubles the warps per SM for the same shared memory.  A pure streaming
+// pass: the draws themselves are made by k_emit.
 template <int DT>
 __device__ __forceinline__ void sample_body(const Params& P) {
     using ST = Stage<DT>;
+    constexpr int NS = SAMPLE_STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bars[SAMPLE_PAIRS * 2];
-    __shared__ float xch[SAMPLE_PAIRS][2][32];  // the odd warp's lane sums, per stage
+    __shared__ __align__(8) uint64_t bars[SAMPLE_PAIRS * NS];
+    __shared__ float xch[SAMPLE_PAIRS][NS][32];  // the odd warp's lane sums, per stage
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pair = warp >> 1, odd = warp & 1;
     WarpStages ws;
-    ws.base = smem + size_t(pair) * 2 * ST::BYTES;
-    ws.bars = bars + pair * 2;
+    ws.base = smem + size_t(pair) * NS * ST::BYTES;
+    ws.bars = bars + pair * NS;
     ws.stage_bytes = ST::BYTES;
     ws.phase = 0;
     ws.inflight = 0;
     ws.broken = false;
-    if (threadIdx.x < SAMPLE_PAIRS * 2) {
+    if (threadIdx.x < SAMPLE_PAIRS * NS) {
         mbar_init(bars + threadIdx.x, 1);
         fence_mbarrier_init();
     }
     __syncthreads();
     griddep_launch_dependents();
     griddep_wait();  // decisions and queues of the acceptance step
+    const int C = P.C;
     const long long W = (long long)gridDim.x * SAMPLE_PAIRS;
     const long long pid = (long long)blockIdx.x * SAMPLE_PAIRS + pair;
-    const long long VT = (long long)P.hdr[HDR_NRES] * P.C;
+    const long long VT = (long long)P.hdr[HDR_NRES] * C;
     const long long r0 = VT * pid / W, r1 = VT * (pid + 1) / W;
-    auto issue_res = [&](long long v, const ReqRec& r, int s) {  // even warp only
-        const int c = int(v % P.C);
-        const int c0 = c * TILE, nel = min(TILE, P.V - c0);
-        const char* l = reinterpret_cast<const char*>(P.logits) +
-                        (((size_t)r.b * P.K1 + r.erow) * P.V + c0) * ST::ESZ;
-        const float* q = P.probs + ((size_t)r.b * P.K + r.erow) * P.V + c0;
-        ws.issue(s, l, uint32_t(nel) * ST::ESZ, q, uint32_t(nel) * 4u, ST::LB);
-    };
     if (r0 < r1) {  // uniform over the pair
+        ReqRec cur = P.res_rec[r0 / C];
+        // producer (even warp): the next unit to copy, its record and stage
+        long long pv = r0;
+        ReqRec prec = cur;
+        int ps = 0;
+        auto issue_next = [&]() {
+            if (odd || pv >= r1) return;
+            const int c = int(pv % C);
+            const int c0 = c * TILE, nel = min(TILE, P.V - c0);
+            const char* l = reinterpret_cast<const char*>(P.logits) +
+                            (((size_t)prec.b * P.K1 + prec.erow) * P.V + c0) * ST::ESZ;
+            const float* q = P.probs + ((size_t)prec.b * P.K + prec.erow) * P.V + c0;
+            ws.issue(ps, l, uint32_t(nel) * ST::ESZ, q, uint32_t(nel) * 4u, ST::LB);
+            ps = ps + 1 == NS ? 0 : ps + 1;
+            if (++pv < r1 && pv % C == 0) prec = P.res_rec[pv / C];
+        };
+#pragma unroll
+        for (int k = 0; k < NS - 1; ++k) issue_next();
         int s = 0;
-        ReqRec cur = P.res_rec[r0 / P.C];
-        if (!odd) issue_res(r0, cur, s);
         for (long long v = r0; v < r1; ++v) {
-            const long long i = v / P.C;
-            const int c = int(v - i * P.C);
-            const long long next = v + 1;
-            ReqRec nxt = cur;
-            if (next < r1) {  // stage s ^ 1 was released by both warps at the last pair barrier
-                if (next / P.C != i) nxt = P.res_rec[next / P.C];
-                if (!odd) issue_res(next, nxt, s ^ 1);
-            }
+            // the stage read at the last pair barrier is refilled first
+            issue_next();
             const bool ok = ws.wait(s);
             // a stage that did not land is still read (in bounds) but its sum is dropped
+            const int c = int(v % C);
             const int nel = min(TILE, P.V - c * TILE);
             const float part = isfinite(offset_of(cur.m, cur.kappa))
                                    ? staged_residual_half<DT, true>(ws.buf(s), nel, cur, odd)
@@ -552,10 +557,10 @@ __device__ __forceinline__ void sample_body(const Params& P) {
             }
             if (!odd) {
                 const float sum = warp_sum_f(__fadd_rn(part, xch[pair][s][lane]));
-                if (lane == 0) P.rsum[(size_t)i * P.C + c] = sum;
+                if (lane == 0) P.rsum[v] = sum;  // entry v / C, chunk c
             }
-            cur = nxt;
-            s ^= 1;
+            if (v + 1 < r1 && (v + 1) % C == 0) cur = P.res_rec[(v + 1) / C];
+            s = s + 1 == NS ? 0 : s + 1;
         }
     }
     finish_stages(P, ws);  // the even warp waits for its copies still in flight
