@@ -227,21 +227,32 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 // Token weights are w(x) = 2^((l(x) - m) kappa) for a reference maximum m.
 // With the offset c = RN(m * kappa) the exponent is one FFMA, l * kappa - c
-// (the product is exact inside the FMA).  Every kernel that computes weights
-// of the same tokens uses the same m, hence the same c, so the rounding of c
-// is a common factor that cancels in every normalised quantity.  When c is
-// not finite (absurdly small T) the two-operation form (l - m) * kappa is
-// used instead; both forms give 2^0 at l == m and 0 far below it.
+// (the product is exact inside the FMA); every weight of that reference then
+// carries the common factor 2^(m kappa - c), which cancels in every
+// normalised quantity.  The factor stays within 2^(+-1/2) while |c| < 2^24
+// (the rounding error of c is at most half an ulp <= 1/2); for larger |c|
+// (very small T, or very large logits) it would overflow or vanish, so the
+// two-operation form (l - m) * kappa, with no factor, is used instead.  Both
+// forms give 2^0 at l == m (up to the factor) and 0 far below it.
+constexpr float OFFSET_LIMIT = 16777216.f;  // 2^24
 __device__ __forceinline__ float offset_of(float m, float kappa) { return __fmul_rn(m, kappa); }
+__device__ __forceinline__ bool offset_ok(float c) { return fabsf(c) < OFFSET_LIMIT; }
 __device__ __forceinline__ float weight_arg(float l, float m, float c, float kappa) {
-    return isfinite(c) ? fmaf(l, kappa, -c) : __fmul_rn(__fsub_rn(l, m), kappa);
+    return offset_ok(c) ? fmaf(l, kappa, -c) : __fmul_rn(__fsub_rn(l, m), kappa);
 }
-// Exponent of the factor 2^((m_c - m) kappa) that rebases weights computed
-// against m_c onto m, consistent with weight_arg.
+// Exponent of the factor that rebases weights computed against m_c onto m,
+// each reference with or without its offset as offset_ok decides: the exact
+// (m_c - m) kappa, less the factor 2^(m_c kappa - c_c) the weights of m_c
+// carry, plus the factor 2^(m kappa - c_m) those of m carry (both exact by
+// FMA).  With both offsets this is c_c - c_m.
 __device__ __forceinline__ float rebase_arg(float m_c, float m, float kappa) {
     const float cc = offset_of(m_c, kappa), cm = offset_of(m, kappa);
-    return (isfinite(cc) && isfinite(cm)) ? __fsub_rn(cc, cm)
-                                          : __fmul_rn(__fsub_rn(m_c, m), kappa);
+    const bool okc = offset_ok(cc), okm = offset_ok(cm);
+    if (okc && okm) return __fsub_rn(cc, cm);
+    float r = __fmul_rn(__fsub_rn(m_c, m), kappa);
+    if (okc) r = __fsub_rn(r, fmaf(m_c, kappa, -cc));
+    if (okm) r = __fadd_rn(r, fmaf(m, kappa, -cm));
+    return r;
 }
 
 // Packed bf16x2 maximum (NaN operands lose).

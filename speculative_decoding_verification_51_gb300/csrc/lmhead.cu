@@ -393,11 +393,11 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                             c_run = offset_of(pm, kappa);
                         }
                         float zs = 0.f;
-                        if (isfinite(c_run)) {
+                        if (offset_ok(c_run)) {
 #pragma unroll
                             for (int k = 0; k < 32; ++k)
                                 if (k < lim) zs = __fadd_rn(zs, ex2_approx(fmaf(f[k], kappa, -c_run)));
-                        } else {  // offset overflows (absurdly small T): (l - max) * kappa
+                        } else {  // offset too large (very small T): (l - max) * kappa
 #pragma unroll
                             for (int k = 0; k < 32; ++k)
                                 if (k < lim)

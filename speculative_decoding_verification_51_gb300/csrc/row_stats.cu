@@ -284,7 +284,7 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
             if (lmax != -INFINITY) {
                 const float cl = offset_of(lmax, rc.kappa);
                 float zs[VPL];
-                if (isfinite(cl)) {  // one FFMA + ex2 per token
+                if (offset_ok(cl)) {  // one FFMA + ex2 per token
 #pragma unroll
                     for (int k = 0; k < VPL; ++k) {
                         float f[EPV];
@@ -297,7 +297,7 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
                             for (int e = 0; e < h; ++e) f[e] = __fadd_rn(f[e], f[e + h]);
                         zs[k] = f[0];
                     }
-                } else {  // offset overflows (absurdly small T): (l - max) * kappa
+                } else {  // offset too large (very small T): (l - max) * kappa
 #pragma unroll
                     for (int k = 0; k < VPL; ++k) {
                         float f[EPV];

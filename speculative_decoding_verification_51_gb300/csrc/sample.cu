@@ -349,8 +349,8 @@ __device__ __forceinline__ void emit_from_p(const Params& P, const ReqRec& rec, 
 // `odd` of the pair takes k = odd, odd + 2, odd + 4, odd + 6, sums each
 // group's 8 weights pairwise in float32, then (k, k + 4) pairs and the two
 // pair sums.  The even warp's value plus the odd warp's, summed over the lanes,
-// is the pairwise sum of the lane's 8 groups.  FIN: the row offset is finite
-// (the weight exponent is one FFMA, as weight_arg computes it then).
+// is the pairwise sum of the lane's 8 groups.  FIN: the row offset passes
+// offset_ok (the weight exponent is then one FFMA, as weight_arg computes it).
 template <int DT, bool FIN>
 __device__ __forceinline__ float staged_residual_half(const uint8_t* st, int nel,
                                                       const ReqRec& rec, int odd) {
@@ -547,7 +547,7 @@ __device__ __forceinline__ void sample_body(const Params& P) {
             // a stage that did not land is still read (in bounds) but its sum is dropped
             const int c = int(v % C);
             const int nel = min(TILE, P.V - c * TILE);
-            const float part = isfinite(offset_of(cur.m, cur.kappa))
+            const float part = offset_ok(offset_of(cur.m, cur.kappa))
                                    ? staged_residual_half<DT, true>(ws.buf(s), nel, cur, odd)
                                    : staged_residual_half<DT, false>(ws.buf(s), nel, cur, odd);
             if (odd) xch[pair][s][lane] = part;

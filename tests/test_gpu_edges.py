@@ -284,3 +284,44 @@ def test_device_seed_and_graph_replay():
         call(s=sd)
         torch.cuda.synchronize()
         assert torch.equal(got[0], out) and torch.equal(got[1], nacc), sd
+
+
+def _tiny_temperature_workload(bf16: bool):
+    """Rows whose offsets RN(max * log2(e) / T) run far past 2^24: tiny
+    temperatures, maxima of both signs and of larger magnitude, and exact
+    ties at the maximum in some rows."""
+    rng = np.random.default_rng(29 + bf16)
+    B, K, V = 40, 3, 5000
+    l = rng.normal(0, 3.0, (B, K + 1, V))
+    l += rng.choice([-60.0, -2.0, 0.0, 35.0], (B, 1, 1))
+    for b in range(0, B, 3):  # two or three tokens share the maximum
+        for j in range(K + 1):
+            top = l[b, j].max() + 1.0
+            l[b, j, rng.choice(V, 2 + (b % 2), replace=False)] = top
+    dl = l[:, :K] + rng.normal(0, 1.0, (B, K, V))
+    q = np.exp(dl - dl.max(-1, keepdims=True))
+    q /= q.sum(-1, keepdims=True)
+    ids = np.array([[l[b, j].argmax() if (b + j) % 2 == 0 else rng.choice(V, p=q[b, j])
+                     for j in range(K)] for b in range(B)])
+    n = rng.integers(0, K + 1, B)
+    temps = [1e-3, 1e-6, 1e-8, 1e-10, 1e-20, 1e-30, 1e-38, 1e-44]
+    T = np.array([temps[b % len(temps)] for b in range(B)])
+    return l, q, ids, n, T
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_tiny_temperatures_match_oracle(bf16):
+    """Very small positive temperatures make softmax(l / T) a point mass on
+    the row's maxima; the one-FFMA weight offset must not overflow there."""
+    l, q, ids, n, T = _tiny_temperature_workload(bf16)
+    w = custom_workload(l, q, ids, n, T, bf16=bf16, seed=7)
+    rep = check_parity(w, f"tiny_T_{'bf16' if bf16 else 'f32'}")
+    assert not rep.failures, rep.failures[:5]
+    assert rep.max_p_rel <= 1e-5
+    # where p is a point mass, every emitted token is one of the row's maxima
+    out, nacc, _, _ = run_gpu(w)
+    lv = w.target_logits.float().cpu().numpy()
+    for b in range(len(n)):
+        if T[b] <= 1e-8 and nacc[b] >= 0:
+            row = lv[b, nacc[b]]
+            assert row[out[b, nacc[b]]] == row.max(), b
