@@ -136,3 +136,15 @@ def test_tree_request_offset():
     assert np.array_equal(sids.cpu().numpy(), ids[sl])
     assert np.array_equal(snacc.cpu().numpy(), nacc[sl])
     assert np.array_equal(slast.cpu().numpy(), last[sl])
+
+
+def test_tree_tiny_temperatures():
+    """Temperatures far below 1 (point masses on the maxima) through the tree
+    walk's merges, acceptances and sibling residuals."""
+    B = 40
+    w = make_tree_workload(B, 8, 5000, bf16=True, seed=77, width=0.6)
+    temps = [1e-3, 1e-8, 1e-10, 1e-20, 1e-30, 1e-38, 1e-44, 0.0]
+    w.temp = torch.tensor([temps[b % len(temps)] for b in range(B)], dtype=torch.float32,
+                          device=w.temp.device)
+    rep, _ = _check(w, "tree_tiny_T")
+    assert rep.sampling > 0 and rep.greedy > 0

@@ -123,3 +123,20 @@ def test_typical_emission_law():
     p /= p.sum()
     obs = np.bincount(out[:, 0], minlength=V)
     assert chisquare(obs, p * B).pvalue > 1e-4
+
+
+def test_typical_tiny_temperatures():
+    """Point-mass target rows (temperatures down to 1e-44): a draft is kept
+    iff it is one of its row's maxima and their share passes the threshold."""
+    rng = np.random.default_rng(17)
+    B, K, V = 40, 3, 5000
+    logits = rng.normal(0, 3, (B, K + 1, V)).astype(np.float32)
+    logits += rng.choice([-60.0, 0.0, 35.0], (B, 1, 1)).astype(np.float32)
+    ids = np.where(rng.random((B, K)) < 0.6, logits[:, :K].argmax(-1),
+                   rng.integers(0, V, (B, K))).astype(np.int32)
+    num = rng.integers(0, K + 1, B).astype(np.int32)
+    temps = [1e-3, 1e-8, 1e-10, 1e-20, 1e-30, 1e-38, 1e-44]
+    temp = np.array([temps[b % len(temps)] for b in range(B)], np.float32)
+    w = custom_workload(logits, None, ids, num, temp, bf16=True, seed=5)
+    rep, _, _ = check_parity_typical(w, 0.05, "typical_tiny_T")
+    _assert_ok(rep)
