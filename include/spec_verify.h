@@ -79,7 +79,10 @@ size_t spec_verify_workspace_size(int B, int K, int V);
  *                    aligned.  Row (b, j) is the target model's logits for the
  *                    position that drafted token j would fill; row K (or row
  *                    num_draft[b]) is the bonus position.  Rows j > num_draft[b]
- *                    are never read.
+ *                    are never read.  Each logit is finite or -inf (a
+ *                    masked token); +inf and NaN logits are outside the
+ *                    contract (the row's outputs are then unspecified, and
+ *                    no kernel indexes memory by a logit value).
  *   draft_probs      [B, K, V] float32, 16-byte aligned: the draft
  *                    distribution q_j that drew draft token j, used as given
  *                    (not renormalised).  Only row e_b (the first rejected
