@@ -325,3 +325,31 @@ def test_tiny_temperatures_match_oracle(bf16):
         if T[b] <= 1e-8 and nacc[b] >= 0:
             row = lv[b, nacc[b]]
             assert row[out[b, nacc[b]]] == row.max(), b
+
+
+def _wide_vocab_workload(bf16: bool, V: int = 300008, B: int = 12, K: int = 3, seed: int = 41):
+    """More than 128 chunks of 2048 tokens per row (V = 300008: 147 chunks,
+    the last one 1000 tokens): the pairwise row merges and the block-by-block
+    chunk picks that shorter vocabularies never reach."""
+    rng = np.random.default_rng(seed + bf16)
+    l = rng.normal(0, 2.0, (B, K + 1, V))
+    dl = l[:, :K] + rng.normal(0, 1.0, (B, K, V))
+    q = np.exp(dl - dl.max(-1, keepdims=True))
+    q /= q.sum(-1, keepdims=True)
+    ids = np.array([[rng.choice(V, p=q[b, j]) for j in range(K)] for b in range(B)])
+    n = rng.integers(0, K + 1, B)
+    n[:2] = K  # at least two requests can reach the bonus row
+    T = np.where(np.arange(B) % 4 == 3, 0.0, rng.uniform(0.5, 1.5, B))
+    return custom_workload(l, q, ids, n, T, bf16=bf16, seed=seed)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_more_than_128_chunks(bf16):
+    w = _wide_vocab_workload(bf16)
+    rep = check_parity(w, f"wide_V300008_{'bf16' if bf16 else 'f32'}")
+    assert not rep.failures, rep.failures[:5]
+    assert rep.max_p_rel <= 1e-5
+    # the early exit merges its rows inside k_row_stats: same outputs
+    par = run_gpu(w)
+    ee = run_gpu(w, early_exit=True)
+    assert np.array_equal(par[0], ee[0]) and np.array_equal(par[1], ee[1])

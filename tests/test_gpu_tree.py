@@ -148,3 +148,11 @@ def test_tree_tiny_temperatures():
                           device=w.temp.device)
     rep, _ = _check(w, "tree_tiny_T")
     assert rep.sampling > 0 and rep.greedy > 0
+
+
+def test_tree_more_than_128_chunks():
+    """V = 300008 (147 chunks of 2048 tokens): the walk's row merges and chunk
+    picks past 128 chunks."""
+    w = make_tree_workload(8, 6, 300008, bf16=True, seed=91, width=0.5)
+    rep, _ = _check(w, "tree_V300008")
+    assert rep.sampling > 0
