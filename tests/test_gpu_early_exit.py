@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_common import check_parity, ensure_built, run_gpu
+from gpu_common import check_parity, custom_workload, ensure_built, run_gpu
 from speculative_decoding_verification_51_gb300 import binding
 from speculative_decoding_verification_51_gb300 import workloads as W
 
@@ -155,3 +155,23 @@ def test_early_exit_graph_replay_with_device_seed():
                                         w.num_draft, w.temperature, seed)
         torch.cuda.synchronize()
         assert torch.equal(ids, out_ids) and torch.equal(nacc, out_nacc)
+
+
+def test_early_exit_31_drafts():
+    """K = 31, the largest draft count: 32 passes, drafts mostly the row
+    argmax so that long accepted prefixes reach the late passes."""
+    rng = np.random.default_rng(31)
+    B, K, V = 24, 31, 3000
+    l = rng.normal(0, 1.5, (B, K + 1, V))
+    q = rng.dirichlet(np.ones(V), (B, K))
+    ids = l[:, :K].argmax(-1)
+    ids[::5, 20] = rng.integers(0, V, (B + 4) // 5)  # some late rejections
+    q[np.arange(B)[:, None], np.arange(K)[None], ids] = 1e-4
+    n = np.where(np.arange(B) % 3 == 0, K, rng.integers(0, K + 1, B))
+    T = np.where(np.arange(B) % 4 == 0, 0.0, 0.2)
+    w = custom_workload(l, q, ids, n, T, bf16=True, seed=31)
+    par, ee = _both(w)
+    _assert_same(w, par, ee)
+    assert par[1].max() >= 20  # some request got past pass 20
+    rep = check_parity(w, "early_exit_K31", early_exit=True)
+    assert not rep.failures, rep.failures[:5]

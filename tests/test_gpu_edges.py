@@ -353,3 +353,22 @@ def test_more_than_128_chunks(bf16):
     par = run_gpu(w)
     ee = run_gpu(w, early_exit=True)
     assert np.array_equal(par[0], ee[0]) and np.array_equal(par[1], ee[1])
+
+
+def test_many_requests_small_vocabulary():
+    """B = 5000 requests (several passes of k_plan's scan, 5000 acceptance
+    CTAs, 10000 draw slots) over a 1024-token vocabulary."""
+    rng = np.random.default_rng(43)
+    B, K, V = 5000, 2, 1024
+    l = rng.normal(0, 2.0, (B, K + 1, V))
+    dl = l[:, :K] + rng.normal(0, 0.7, (B, K, V))
+    q = np.exp(dl - dl.max(-1, keepdims=True))
+    q /= q.sum(-1, keepdims=True)
+    cq = q.cumsum(-1)
+    ids = (cq < rng.random((B, K, 1))).sum(-1).clip(0, V - 1)  # x_j ~ q_j
+    n = rng.integers(0, K + 1, B)
+    T = np.where(rng.random(B) < 0.2, 0.0, rng.uniform(0.5, 1.5, B))
+    w = custom_workload(l, q, ids, n, T, bf16=True, seed=43)
+    rep = check_parity(w, "B5000_V1024")
+    assert not rep.failures, rep.failures[:5]
+    assert rep.excused <= max(1, 0.01 * rep.sampling), rep.summary()
