@@ -99,9 +99,10 @@ import oracle  # noqa: E402
 from speculative_decoding_verification_51_gb300 import workloads as W  # noqa: E402
 
 
-def _fused_check(B, K, V, H, seed, **kw):
+def _fused_check(B, K, V, H, seed, w=None, **kw):
     ensure_built()
-    w = W.make_lmhead_workload(B, K, V, H, seed=seed, **kw)
+    if w is None:
+        w = W.make_lmhead_workload(B, K, V, H, seed=seed, **kw)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     ids, nacc, logits, rows, req = binding.spec_verify_lmhead(
         w.hidden, w.lm_head, w.draft_probs, w.draft_ids, w.num_draft, w.temperature, w.seed,
@@ -142,3 +143,15 @@ def test_fused_verify_largest_vocabulary():
     25% greedy) with hidden size 1024."""
     rep = _fused_check(256, 3, 151936, 1024, seed=4)
     assert rep.greedy > 0 and rep.sampling > 0
+
+
+def test_fused_verify_tiny_temperatures():
+    """The projection epilogue's running row statistics at temperatures down
+    to 1e-44 (offsets RN(max * log2(e) / T) far past 2^24)."""
+    B, K, V, H = 32, 3, 4104, 128
+    w = W.make_lmhead_workload(B, K, V, H, seed=71, greedy_frac=0.2)
+    temps = torch.tensor([1e-3, 1e-8, 1e-10, 1e-20, 1e-30, 1e-38, 1e-44, 0.7])
+    t = temps[torch.arange(B) % len(temps)].to(w.temperature.device)
+    w.temperature = torch.where(w.temperature > 0, t, w.temperature).contiguous()
+    rep = _fused_check(B, K, V, H, seed=71, w=w)
+    assert rep.sampling > 0
