@@ -372,3 +372,28 @@ def test_many_requests_small_vocabulary():
     rep = check_parity(w, "B5000_V1024")
     assert not rep.failures, rep.failures[:5]
     assert rep.excused <= max(1, 0.01 * rep.sampling), rep.summary()
+
+
+def test_residual_without_mass_falls_back_to_p():
+    """q_j = 2 p_j on every row (a draft distribution that is not normalised):
+    a rejected draft leaves max(0, p - q) = 0 everywhere, and the token at the
+    rejected row is drawn from p with the row's emission uniform instead."""
+    rng = np.random.default_rng(53)
+    B, K, V = 48, 3, 3000
+    l = rng.normal(0, 2.0, (B, K + 1, V)).astype(np.float32)
+    T = rng.uniform(0.6, 1.4, B)
+    z = l[:, :K].astype(np.float64) / T[:, None, None]
+    p = np.exp(z - z.max(-1, keepdims=True))
+    p /= p.sum(-1, keepdims=True)
+    q = (2.0 * p).astype(np.float32)
+    cp = p.cumsum(-1)
+    ids = (cp < rng.random((B, K, 1))).sum(-1).clip(0, V - 1)  # x_j ~ p_j
+    n = np.full(B, K)
+    w = custom_workload(l, q, ids, n, T, bf16=False, seed=53)
+    rep = check_parity(w, "zero_residual_fallback")
+    assert not rep.failures, rep.failures[:5]
+    _, nacc, _, req = run_gpu(w)
+    rejected = nacc < n
+    assert rejected.sum() >= 10
+    assert (req[rejected, 0] == oracle.MODE_FALLBACK).all()
+    assert (req[~rejected, 0] == oracle.MODE_BONUS).all()
