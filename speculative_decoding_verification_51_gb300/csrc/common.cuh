@@ -57,7 +57,9 @@ static_assert(SAMPLE_STAGES >= 2 && SAMPLE_PAIRS * SAMPLE_STAGES <= 32, "k_sampl
 constexpr int PLAN_THREADS = 1024;
 
 // HDR_ROUND + r: rows of early-exit round r (r >= 1), listed at rowlist + r * B
-enum { HDR_ROWS = 0, HDR_NRES = 1, HDR_NBONUS = 2, HDR_STATUS = 3, HDR_ROUND = 8, HDR_INTS = 64 };
+// HDR_CLAIM: tail segments claimed so far in the all-rows pass of k_row_stats
+enum { HDR_ROWS = 0, HDR_NRES = 1, HDR_NBONUS = 2, HDR_STATUS = 3, HDR_CLAIM = 4, HDR_ROUND = 8,
+       HDR_INTS = 64 };
 static_assert(HDR_ROUND + SPEC_MAX_K + 1 <= HDR_INTS, "round counters overflow the header");
 enum { MODE_BAD = -1, MODE_GREEDY = 0, MODE_RESIDUAL = 1, MODE_BONUS = 2, MODE_FALLBACK = 3,
        MODE_TYPICAL = 4 };

@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_plan(Params P) {
     if (tid == 0) {
         P.hdr[HDR_NRES] = 0;
         P.hdr[HDR_NBONUS] = 0;
+        P.hdr[HDR_CLAIM] = 0;
         *P.status = 0;
         carry = 0;
     }

@@ -103,9 +103,9 @@ struct RowCtx {
     int xchunk;    // chunk holding xj (-1: none)
 };
 
-__device__ __forceinline__ RowCtx row_ctx(const Params& P, const int* rowlist, long long r) {
+__device__ __forceinline__ RowCtx row_ctx(const Params& P, int slot) {
     RowCtx rc;
-    rc.slot = rowlist[r];
+    rc.slot = slot;
     const int b = rc.slot / P.K1, j = rc.slot - b * P.K1;
     rc.b = b;
     rc.n = P.num_draft[b];
@@ -121,8 +121,260 @@ __device__ __forceinline__ RowCtx row_ctx(const Params& P, const int* rowlist, l
     rc.xchunk = x >= 0 ? x / TILE : -1;
     return rc;
 }
+__device__ __forceinline__ RowCtx row_ctx(const Params& P, const int* rowlist, long long r) {
+    return row_ctx(P, rowlist[r]);
+}
 
 }  // namespace
+
+// The statistics of one staged tile (d: this lane's VPL vectors, nvec valid
+// vectors, tok0 the tile's first token): greedy rows the tile max and the
+// lowest index attaining it; sampling rows the tile max and the sum of
+// 2^(l kappa - c) against the tile max's offset c (see weight_arg).
+template <int DT>
+__device__ __forceinline__ Partial tile_partial(const uint4 (&d)[Tile<DT>::VPL], int nvec, int tok0,
+                                                const RowCtx& rc) {
+    constexpr int EPV = Tile<DT>::EPV, VPL = Tile<DT>::VPL;
+    const int lane = threadIdx.x & 31;
+    const float lmax = lane_max<DT>(d);
+    Partial out;
+    if (rc.greedy) {
+        // lowest index attaining the tile max: visiting tokens from high to
+        // low index leaves the lowest hit
+        const float m = redux_max_f32(lmax);
+        int bidx = INT_MAX;
+#pragma unroll
+        for (int k = VPL - 1; k >= 0; --k) {
+            if (k * 32 + lane < nvec) {
+                float f[EPV];
+                unpack<DT>(d[k], f);
+#pragma unroll
+                for (int e = EPV - 1; e >= 0; --e)
+                    if (f[e] == m) bidx = tok0 + (k * 32 + lane) * EPV + e;
+            }
+        }
+        out.m = m;
+        out.amax = redux_min_s32(bidx);
+        out.z = 0.0;
+    } else {
+        // each lane sums against its own maximum, so the ex2 loop does not
+        // wait for the warp-wide maximum; one rescale per lane follows
+        float zl = 0.f;
+        if (lmax != -INFINITY) {
+            const float cl = offset_of(lmax, rc.kappa);
+            float zs[VPL];
+            if (offset_ok(cl)) {  // one FFMA + ex2 per token
+#pragma unroll
+                for (int k = 0; k < VPL; ++k) {
+                    float f[EPV];
+                    unpack<DT>(d[k], f);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) f[e] = ex2_approx(fmaf(f[e], rc.kappa, -cl));
+#pragma unroll
+                    for (int h = EPV / 2; h; h >>= 1)
+#pragma unroll
+                        for (int e = 0; e < h; ++e) f[e] = __fadd_rn(f[e], f[e + h]);
+                    zs[k] = f[0];
+                }
+            } else {  // offset too large (very small T): (l - max) * kappa
+#pragma unroll
+                for (int k = 0; k < VPL; ++k) {
+                    float f[EPV];
+                    unpack<DT>(d[k], f);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e)
+                        f[e] = ex2_approx(__fmul_rn(__fsub_rn(f[e], lmax), rc.kappa));
+#pragma unroll
+                    for (int h = EPV / 2; h; h >>= 1)
+#pragma unroll
+                        for (int e = 0; e < h; ++e) f[e] = __fadd_rn(f[e], f[e + h]);
+                    zs[k] = f[0];
+                }
+            }
+#pragma unroll
+            for (int h = VPL / 2; h; h >>= 1)
+#pragma unroll
+                for (int k = 0; k < h; ++k) zs[k] = __fadd_rn(zs[k], zs[k + h]);
+            zl = zs[0];
+        }
+        const float m = redux_max_f32(lmax);
+        if (zl != 0.f) zl = __fmul_rn(zl, ex2_approx(rebase_arg(lmax, m, rc.kappa)));
+        out.m = m;
+        out.amax = -1;
+        out.z = double(warp_sum_f(zl));
+    }
+    return out;
+}
+
+
+// The all-rows pass (and a tree pass), balanced across SMs.  The streaming
+// speed of a warp depends on where its SM sits (measured: warps of an equal
+// static split ended between 29 and 44 us on the largest-vocabulary workload,
+// the same SMs slow in every run), so an equal split leaves a tail.  Warp w
+// streams the first 7/8 of its equal range [T w / W, T (w + 1) / W) as a
+// static segment, and the last 1/8 of every range is handed out as one
+// segment per claim: claim k (one atomic on a counter k_plan cleared, fired
+// a few tiles before the claimer runs out of work, so in about the order in
+// which warps finish) takes the tail of warp (k * CLAIM_STRIDE) mod W; the
+// stride is a prime above any warp count, so the claims take every tail
+// exactly once and consecutive claims land far apart in the logits.  The
+// producer lane passes each staged tile's row slot and chunk to the
+// consumer through shared memory, with the tiles left in its segment.
+#ifndef SV_TAIL_DEN
+#define SV_TAIL_DEN 8
+#endif
+#ifndef SV_FIRE_AHEAD
+#define SV_FIRE_AHEAD 2
+#endif
+constexpr int TAIL_DEN = SV_TAIL_DEN;        // the claimed tail is 1/TAIL_DEN of each range
+constexpr long long CLAIM_STRIDE = 1000003;  // prime
+constexpr int FIRE_AHEAD = SV_FIRE_AHEAD;    // tiles left when the next claim goes out
+
+template <int DT>
+__device__ __forceinline__ void stream_balanced(const Params& P, uint8_t* buf,
+                                                uint64_t (*bars)[STATS_STAGES], const int* rowlist,
+                                                long long T, long long W, long long w) {
+    using TL = Tile<DT>;
+    constexpr int EPV = TL::EPV, VPL = TL::VPL;
+    __shared__ int4 sinfo[STATS_WARPS][STATS_STAGES];  // {slot, chunk, tiles left in segment, segment start}
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = P.C;
+
+    // ---- producer state (lane 0)
+    const long long t0 = T * w / W, t1 = T * (w + 1) / W;
+    long long pt = t0, pe = t1 - (t1 - t0) / TAIL_DEN;  // the static segment
+    bool seg_first = true;  // the next issued tile starts a segment
+    bool fired = false;     // a claim is in flight for the next segment
+    int claim = 0;
+    bool done = false;
+    int issued = 0;
+    long long prow = -1;
+    int pslot = 0;
+    auto fire = [&]() {
+        claim = atomicAdd(P.hdr + HDR_CLAIM, 1);
+        fired = true;
+    };
+    // lane 0: move to the next claimed tail; false when every tail is taken
+    auto next_segment = [&]() -> bool {
+        for (;;) {
+            if (!fired) fire();
+            fired = false;
+            if (claim >= W) return false;
+            const long long v = ((long long)claim * CLAIM_STRIDE) % W;
+            const long long a = T * v / W, b = T * (v + 1) / W;
+            const long long tail = (b - a) / TAIL_DEN;
+            if (tail > 0) {
+                pt = b - tail;
+                pe = b;
+                seg_first = true;
+                return true;
+            }
+        }
+    };
+    auto issue = [&](int s) {
+        if (done) return;
+        while (pt == pe)
+            if (!next_segment()) {
+                done = true;
+                return;
+            }
+        if (!fired && pe - pt <= FIRE_AHEAD) fire();
+        const long long r = pt / C;
+        const int c = int(pt - r * C);
+        if (r != prow) {
+            prow = r;
+            pslot = rowlist[r];
+        }
+        const int nel = min(TILE, P.V - c * TILE);
+        const uint32_t bytes = uint32_t(nel) * TL::ESZ;
+        const char* src = reinterpret_cast<const char*>(P.logits) +
+                          ((size_t)pslot * P.V + (size_t)c * TILE) * TL::ESZ;
+        sinfo[warp][s] = make_int4(pslot, c, int(pe - pt - 1), seg_first ? 1 : 0);
+        seg_first = false;
+        mbar_arrive_expect_tx(&bars[warp][s], bytes);
+        bulk_g2s(buf + s * TL::BYTES, src, bytes, &bars[warp][s]);
+        ++pt;
+        ++issued;
+    };
+    if (lane == 0)
+        for (int k = 0; k < STATS_STAGES; ++k) issue(k);
+
+    // ---- consumer (whole warp)
+    RowCtx rc;
+    rc.slot = -1;
+    float qx = 0.f;
+    long long i = 0;
+    int s = 0;
+    uint32_t parity = 0;
+    bool timed_out = false;
+    int have = 0;
+    for (;; ++i) {
+        have = __shfl_sync(0xffffffffu, issued, 0);
+        if (i >= have) break;
+        const bool landed = mbar_wait_bounded(&bars[warp][s], parity);
+        if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform exit
+            timed_out = true;
+            break;
+        }
+        const int4 si = sinfo[warp][s];
+        const int cc = si.y;
+        if (si.x != rc.slot || si.w) {
+            if (si.x != rc.slot) rc = row_ctx(P, si.x);
+            // q_j(x_j) is fetched by the warp whose segment holds x_j's tile
+            if (P.rule == RULE_LOSSLESS && rc.xj >= 0 && rc.xchunk >= cc &&
+                rc.xchunk - cc <= si.z && lane == 0) {
+                const int b = rc.slot / P.K1, j = rc.slot - b * P.K1;
+                qx = __ldg(P.probs + ((size_t)b * P.K + j) * P.V + rc.xj);
+            }
+        }
+        const int nvec = min(TILE, P.V - cc * TILE) / EPV;
+        const uint8_t* stage = buf + s * TL::BYTES;
+        const uint4* v4 = reinterpret_cast<const uint4*>(stage);
+        uint4 d[VPL];
+        if (nvec == TILE / EPV) {
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) d[k] = v4[k * 32 + lane];
+        } else {  // the row's ragged last chunk: pad with -inf
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                const int v = k * 32 + lane;
+                d[k] = v < nvec ? v4[v]
+                                : make_uint4(TL::NEG_INF_WORD, TL::NEG_INF_WORD,
+                                             TL::NEG_INF_WORD, TL::NEG_INF_WORD);
+            }
+        }
+        const bool has_x = (cc == rc.xchunk);
+        float lx = 0.f;
+        if (has_x && lane == 0) {
+            const int e = rc.xj - cc * TILE;
+            if constexpr (DT == SPEC_BF16)
+                lx = __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(stage)[e]) << 16);
+            else
+                lx = reinterpret_cast<const float*>(stage)[e];
+        }
+        __syncwarp();  // every lane holds its share: the stage can be refilled
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            issue(s);
+        }
+        const Partial out = tile_partial<DT>(d, nvec, cc * TILE, rc);
+        if (lane == 0) {
+            P.part[(size_t)rc.slot * C + cc] = out;
+            if (has_x) P.gath[rc.slot] = make_float2(lx, qx);
+        }
+        if (++s == STATS_STAGES) {
+            s = 0;
+            parity ^= 1u;
+        }
+    }
+    if (timed_out) {
+        if (lane == 0) atomicOr(P.status, int(SPEC_BADBIT_TIMEOUT));
+        // let the copies still in flight land before the CTA's shared memory is released
+        for (long long u = i; u < have && u < i + STATS_STAGES; ++u)
+            mbar_wait_bounded(&bars[warp][int(u % STATS_STAGES)], uint32_t((u / STATS_STAGES) & 1),
+                              100000000ull);
+    }
+}
 
 template <int DT>
 __device__ __forceinline__ void row_stats_body(const Params& P) {
@@ -149,6 +401,10 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
     const long long T = R * P.C;
     const long long W = (long long)gridDim.x * STATS_WARPS;
     const long long w = (long long)blockIdx.x * STATS_WARPS + warp;
+    if (P.round < 0) {  // the all-rows pass: balanced across SMs
+        stream_balanced<DT>(P, buf, bars, rowlist, T, W, w);
+        return;
+    }
     const long long t0 = T * w / W, t1 = T * (w + 1) / W;
     if (t0 >= t1) return;
     const long long r0 = t0 / P.C;
@@ -256,74 +512,7 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
             issue(s);
         }
 
-        const int tok0 = cc * TILE;
-        const float lmax = lane_max<DT>(d);
-        Partial out;
-        if (rc.greedy) {
-            // lowest index attaining the tile max: visiting tokens from high to
-            // low index leaves the lowest hit
-            const float m = redux_max_f32(lmax);
-            int bidx = INT_MAX;
-#pragma unroll
-            for (int k = VPL - 1; k >= 0; --k) {
-                if (k * 32 + lane < nvec) {
-                    float f[EPV];
-                    unpack<DT>(d[k], f);
-#pragma unroll
-                    for (int e = EPV - 1; e >= 0; --e)
-                        if (f[e] == m) bidx = tok0 + (k * 32 + lane) * EPV + e;
-                }
-            }
-            out.m = m;
-            out.amax = redux_min_s32(bidx);
-            out.z = 0.0;
-        } else {
-            // each lane sums against its own maximum, so the ex2 loop does not
-            // wait for the warp-wide maximum; one rescale per lane follows
-            float zl = 0.f;
-            if (lmax != -INFINITY) {
-                const float cl = offset_of(lmax, rc.kappa);
-                float zs[VPL];
-                if (offset_ok(cl)) {  // one FFMA + ex2 per token
-#pragma unroll
-                    for (int k = 0; k < VPL; ++k) {
-                        float f[EPV];
-                        unpack<DT>(d[k], f);
-#pragma unroll
-                        for (int e = 0; e < EPV; ++e) f[e] = ex2_approx(fmaf(f[e], rc.kappa, -cl));
-#pragma unroll
-                        for (int h = EPV / 2; h; h >>= 1)
-#pragma unroll
-                            for (int e = 0; e < h; ++e) f[e] = __fadd_rn(f[e], f[e + h]);
-                        zs[k] = f[0];
-                    }
-                } else {  // offset too large (very small T): (l - max) * kappa
-#pragma unroll
-                    for (int k = 0; k < VPL; ++k) {
-                        float f[EPV];
-                        unpack<DT>(d[k], f);
-#pragma unroll
-                        for (int e = 0; e < EPV; ++e)
-                            f[e] = ex2_approx(__fmul_rn(__fsub_rn(f[e], lmax), rc.kappa));
-#pragma unroll
-                        for (int h = EPV / 2; h; h >>= 1)
-#pragma unroll
-                            for (int e = 0; e < h; ++e) f[e] = __fadd_rn(f[e], f[e + h]);
-                        zs[k] = f[0];
-                    }
-                }
-#pragma unroll
-                for (int h = VPL / 2; h; h >>= 1)
-#pragma unroll
-                    for (int k = 0; k < h; ++k) zs[k] = __fadd_rn(zs[k], zs[k + h]);
-                zl = zs[0];
-            }
-            const float m = redux_max_f32(lmax);
-            if (zl != 0.f) zl = __fmul_rn(zl, ex2_approx(rebase_arg(lmax, m, rc.kappa)));
-            out.m = m;
-            out.amax = -1;
-            out.z = double(warp_sum_f(zl));
-        }
+        const Partial out = tile_partial<DT>(d, nvec, cc * TILE, rc);
         if (lane == 0) {
             P.part[(size_t)rc.slot * P.C + cc] = out;
             if (has_x) P.gath[rc.slot] = make_float2(lx, qx);
