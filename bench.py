@@ -10,8 +10,9 @@ line (rank 0).
             device-timed with CUDA events around each call; L2 is flushed
             before every timed call (256 MiB written, then another 256 MiB
             read, so that it holds clean unrelated lines).
-  e2e       same metric through spec_verify_host: pinned host inputs copied
-            in, verified, outputs copied back, all inside the timed region.
+  e2e       same metric through spec_verify_host: from pinned host inputs
+            only the rows the verifier reads are copied in, then verified,
+            outputs copied back, all inside the timed region.
   roofline  k_row_stats (the dominant kernel): algorithmic bytes per launch
             (every valid logits row once + one 16-byte partial per
             2048-token chunk) / its CUDA-event duration, against the measured
@@ -806,7 +807,26 @@ def main():
         b_ev.record(stream)
         torch.cuda.synchronize()
         e2e_ms = a_ev.elapsed_time(b_ev) / e2e_steps
-        h2d = sum(t.numel() * t.element_size() for t in h.values())
+        # Pinned (mapped) host buffers take the rows-only path of
+        # spec_verify_host: the logits rows 0..n_b, q_j(x_j) of every draft,
+        # and the q row of each residual draw cross the link (the residual
+        # count of each timed seed is taken from an untimed device call).
+        n_cpu = h["num_draft"].long()
+        valid = (n_cpu >= 0) & (n_cpu <= K)
+        rows = torch.where(valid, n_cpu + 1, torch.ones_like(n_cpu))
+        esz = h["target_logits"].element_size()
+        h2d = int(rows.sum()) * V * esz
+        h2d += sum(t.numel() * t.element_size()
+                   for t in (h["draft_ids"], h["num_draft"], h["temperature"]))
+        if h["draft_probs"] is not None:
+            h2d += int(torch.where(valid, n_cpu, torch.zeros_like(n_cpu)).sum()) * 4
+            samp = (h["temperature"] > 0) & valid
+            n_res = 0
+            for i in range(e2e_steps):
+                _, nacc_i = binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids,
+                                                w.num_draft, w.temperature, 5000 + i)
+                n_res += int(((nacc_i.cpu().long() < n_cpu) & samp & (nacc_i.cpu() >= 0)).sum())
+            h2d += int(round(n_res / e2e_steps)) * V * 4
         d2h = h_out.numel() * 4 + h_nacc.numel() * 4
         e2e = {"value": world * pos / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}

@@ -386,10 +386,16 @@ int32_t* spec_verify_status_ptr(void* workspace);
  * (d_logits [B, K+1, V], d_probs [B, K, V], d_small: at least
  * spec_verify_host_small_bytes(B, K) bytes, 256-byte aligned), the verifier
  * runs, and out_ids / out_num_accepted are copied back, all enqueued on
- * `stream` in that order (one cudaMemcpyAsync per tensor).  Host buffers
- * should be pinned for the copies to be asynchronous; the call does not
- * synchronise, so the host outputs are valid after the stream is synchronised.
- * h_probs / d_probs may be NULL when every request is greedy.
+ * `stream`.  When h_logits (and h_probs) are page-locked and mapped into the
+ * device's address space (cudaHostAlloc / cudaHostRegister memory on a
+ * unified-addressing system), copy kernels move only what the verifier
+ * reads: the logits rows 0..num_draft[b], q_j(x_j) for every draft, and,
+ * once the acceptances are known, the q row of each residual draw; the rest
+ * of d_logits / d_probs is left as it was.  Other host memory is copied
+ * whole (one cudaMemcpyAsync per tensor; pageable memory makes those copies
+ * synchronous).  The call does not synchronise, so the host outputs are
+ * valid after the stream is synchronised.  h_probs / d_probs may be NULL
+ * when every request is greedy.
  */
 size_t spec_verify_host_small_bytes(int B, int K);
 spec_status spec_verify_host(const void* h_logits, spec_dtype logits_dtype, const float* h_probs,

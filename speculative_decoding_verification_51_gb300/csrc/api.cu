@@ -127,7 +127,8 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
                            int32_t* dev_status, cudaEvent_t* events, int rule = RULE_LOSSLESS,
                            float threshold = 0.f, const int32_t* parents = nullptr,
                            int32_t* out_last = nullptr, const uint64_t* seed_dev = nullptr,
-                           bool early_exit = false, const LmHeadIn* lm = nullptr) {
+                           bool early_exit = false, const LmHeadIn* lm = nullptr,
+                           const float* host_probs = nullptr) {
     const bool tree = parents != nullptr;
     if (!sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
     if (rule == RULE_TYPICAL && threshold != threshold) return SPEC_ERR_INVALID_ARG;
@@ -229,6 +230,12 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     // the all-rows pass leaves the acceptances to one warp per request here
     if (!lm && !early_exit && e == cudaSuccess)
         e = launch(k_accept_all, unsigned(B), ACCEPT_WARPS * 32, 0, st, true, P);
+    // spec_verify_host: the q rows of the residual draws, now that they are known
+    if (host_probs && e == cudaSuccess) {
+        const long long g = B < 4LL * dev.sms ? B : 4LL * dev.sms;
+        k_qrows_in<<<unsigned(g > 0 ? g : 1), HOST_IO_THREADS, 0, st>>>(P, host_probs);
+        e = cudaGetLastError();
+    }
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess)
         e = launch(bf16 ? k_sample_bf16 : k_sample_f32, unsigned(g3), SAMPLE_PAIRS * 64,
@@ -398,6 +405,17 @@ spec_status spec_verify(const void* target_logits, spec_dtype logits_dtype,
                           workspace_bytes, stream, 0u, nullptr, nullptr, nullptr);
 }
 
+// The device address of a page-locked host buffer mapped into the device's
+// address space, or nullptr for any other memory.
+static const void* mapped_device_ptr(const void* h) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+        (void)cudaGetLastError();  // not a pointer CUDA knows
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 // Small device buffer of spec_verify_host: ids, num_draft, temperature,
 // out_ids, out_num_accepted, each 256-byte aligned.
 size_t spec_verify_host_small_bytes(int B, int K) {
@@ -434,17 +452,40 @@ spec_status spec_verify_host(const void* h_logits, spec_dtype logits_dtype, cons
     s += align256(b * k1 * 4);
     int32_t* d_nacc = reinterpret_cast<int32_t*>(s);
 
-    cudaError_t e = cudaMemcpyAsync(d_logits, h_logits, b * k1 * V * esz, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess && h_probs)
-        e = cudaMemcpyAsync(d_probs, h_probs, b * K * V * 4, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess && K > 0)
-        e = cudaMemcpyAsync(d_ids, h_draft_ids, b * K * 4, cudaMemcpyHostToDevice, st);
+    // Page-locked host buffers mapped into the device's address space are read
+    // by copy kernels, and only what the verifier reads crosses the link: the
+    // logits rows 0..n_b, q_j(x_j), and the q rows of the residual draws.
+    // Other host memory takes whole-tensor copies.
+    const void* m_logits = mapped_device_ptr(h_logits);
+    const float* m_probs = h_probs ? static_cast<const float*>(mapped_device_ptr(h_probs)) : nullptr;
+    const bool rows_only = m_logits && (!h_probs || m_probs);
+    cudaError_t e = cudaSuccess;
+    if (K > 0) e = cudaMemcpyAsync(d_ids, h_draft_ids, b * K * 4, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(d_num, h_num_draft, b * 4, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(d_temp, h_temperature, b * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && rows_only) {
+        DeviceInfo dev;
+        if (device_info(dev) != SPEC_OK) return SPEC_ERR_CUDA;
+        const long long rows = (long long)B * k1;
+        const long long g = rows < 16LL * dev.sms ? rows : 16LL * dev.sms;
+        k_rows_in<<<unsigned(g), HOST_IO_THREADS, 0, st>>>(m_logits, d_logits, d_num, B, K,
+                                                           size_t(V) * esz);
+        e = cudaGetLastError();
+        if (e == cudaSuccess && h_probs && K > 0) {
+            k_qx_in<<<unsigned(B), 32, 0, st>>>(m_probs, d_probs, d_ids, d_num, B, K, V);
+            e = cudaGetLastError();
+        }
+    } else if (e == cudaSuccess) {
+        e = cudaMemcpyAsync(d_logits, h_logits, b * k1 * V * esz, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess && h_probs)
+            e = cudaMemcpyAsync(d_probs, h_probs, b * K * V * 4, cudaMemcpyHostToDevice, st);
+    }
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
-    const spec_status r = spec_verify(d_logits, logits_dtype, h_probs ? d_probs : nullptr,
-                                      K > 0 ? d_ids : nullptr, d_num, d_temp, seed, B, K, V,
-                                      d_out, d_nacc, workspace, workspace_bytes, stream);
+    const spec_status r = verify_impl(
+        d_logits, logits_dtype, h_probs ? d_probs : nullptr, K > 0 ? d_ids : nullptr, d_num, d_temp,
+        seed, B, K, V, d_out, d_nacc, workspace, workspace_bytes, stream, 0, nullptr, nullptr,
+        nullptr, nullptr, RULE_LOSSLESS, 0.f, nullptr, nullptr, nullptr, false, nullptr,
+        rows_only ? m_probs : nullptr);
     if (r != SPEC_OK) return r;
     e = cudaMemcpyAsync(h_out_ids, d_out, b * k1 * 4, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess)

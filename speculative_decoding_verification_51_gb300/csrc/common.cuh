@@ -354,6 +354,13 @@ __device__ __forceinline__ int warp_max_int(int v) {
 
 // Kernel entry points (defined in the .cu files).
 __global__ void k_plan(Params P);
+// host_io.cu: copies of spec_verify_host from mapped page-locked host memory
+constexpr int HOST_IO_THREADS = 256;
+__global__ void k_rows_in(const void* src, void* dst, const int32_t* num, int B, int K,
+                          size_t row_bytes);
+__global__ void k_qx_in(const float* src, float* dst, const int32_t* ids, const int32_t* num,
+                        int B, int K, int V);
+__global__ void k_qrows_in(Params P, const float* src);
 __global__ void k_row_stats_f32(Params P);
 __global__ void k_row_stats_bf16(Params P);
 __global__ void k_sample_f32(Params P);

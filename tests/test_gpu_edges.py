@@ -186,6 +186,44 @@ def test_host_buffer_entry_point_matches():
     assert np.array_equal(out.numpy(), want[0]) and np.array_equal(nacc.numpy(), want[1])
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_buffer_rows_only_and_whole_copies(pinned):
+    """spec_verify_host on the largest vocabulary (leading 64 requests):
+    pinned host buffers take the copy kernels that move only the rows the
+    verifier reads (the device buffers start as garbage, so a row it reads
+    but did not copy shows); pageable buffers take whole-tensor copies.
+    Both give the device call's outputs."""
+    w = W.make_workload(4, device="cuda").leading(64)
+    want = run_gpu(w, debug=False)
+    B, K1, V = w.target_logits.shape
+    K = K1 - 1
+    h = {k: getattr(w, k).cpu() for k in
+         ("target_logits", "draft_probs", "draft_ids", "num_draft", "temperature")}
+    if pinned:
+        h = {k: t.pin_memory() for k, t in h.items()}
+    out = torch.empty((B, K1), dtype=torch.int32)
+    nacc = torch.empty((B,), dtype=torch.int32)
+    if pinned:
+        out, nacc = out.pin_memory(), nacc.pin_memory()
+    d_l = torch.full_like(w.target_logits, float("nan"))
+    d_p = torch.full_like(w.draft_probs, float("nan"))
+    small = torch.empty(binding.host_small_bytes(B, K), dtype=torch.uint8, device="cuda")
+    ws = binding.new_workspace(B, K, V, "cuda")
+    for seed in (w.seed, w.seed + 1):
+        binding.spec_verify_host(h["target_logits"], h["draft_probs"], h["draft_ids"],
+                                 h["num_draft"], h["temperature"], seed, out, nacc, d_l, d_p,
+                                 small, ws)
+        torch.cuda.synchronize()
+        ref = run_gpu(w, debug=False) if seed == w.seed else None
+        if seed != w.seed:
+            ids2, nacc2 = binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids,
+                                              w.num_draft, w.temperature, seed)
+            torch.cuda.synchronize()
+            ref = (ids2.cpu().numpy(), nacc2.cpu().numpy())
+        assert np.array_equal(out.numpy(), ref[0]) and np.array_equal(nacc.numpy(), ref[1])
+    assert (want[1] < w.num_draft.cpu().numpy()).any()  # residual draws took q rows
+
+
 def test_misaligned_and_small_workspace_rejected():
     ensure_built()
     w = W.make_workload(1, device="cuda")
