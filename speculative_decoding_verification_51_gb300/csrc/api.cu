@@ -90,10 +90,16 @@ constexpr bool kUsePdl = true;
 #else
 constexpr bool kUsePdl = false;
 #endif
+// Launches that use programmatic dependent launch whatever SV_PDL says (bit 0
+// k_row_stats, 1 k_accept_all, 2 k_sample, 3 k_emit).
+#ifndef SV_PDL_MASK
+#define SV_PDL_MASK 0
+#endif
+constexpr unsigned kPdlMask = SV_PDL_MASK;
 
 cudaError_t launch(void (*kern)(Params), unsigned grid, unsigned block, size_t smem,
-                   cudaStream_t st, bool pdl, const Params& P) {
-    pdl = pdl && kUsePdl;
+                   cudaStream_t st, bool pdl, const Params& P, unsigned pdl_bit = 0) {
+    pdl = pdl && (kUsePdl || (kPdlMask & pdl_bit));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
@@ -218,7 +224,7 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
         }
     } else if (e == cudaSuccess) {
         e = launch(bf16 ? k_row_stats_bf16 : k_row_stats_f32, unsigned(g1),
-                   STATS_WARPS * 32, stats_smem(logits_dtype), st, true, P);
+                   STATS_WARPS * 32, stats_smem(logits_dtype), st, true, P, 1u);
     }
     if (e == cudaSuccess) e = mark(2);
     if (tree) {  // the walks, one CTA per request
@@ -229,7 +235,7 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     }
     // the all-rows pass leaves the acceptances to one warp per request here
     if (!lm && !early_exit && e == cudaSuccess)
-        e = launch(k_accept_all, unsigned(B), ACCEPT_WARPS * 32, 0, st, true, P);
+        e = launch(k_accept_all, unsigned(B), ACCEPT_WARPS * 32, 0, st, true, P, 2u);
     // spec_verify_host: the q rows of the residual draws, now that they are known
     if (host_probs && e == cudaSuccess) {
         const long long g = B < 4LL * dev.sms ? B : 4LL * dev.sms;
@@ -239,11 +245,11 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess)
         e = launch(bf16 ? k_sample_bf16 : k_sample_f32, unsigned(g3), SAMPLE_PAIRS * 64,
-                   sample_smem(logits_dtype), st, true, P);
+                   sample_smem(logits_dtype), st, true, P, 4u);
     if (e == cudaSuccess) e = mark(4);
     if (e == cudaSuccess)
         e = launch(bf16 ? k_emit_bf16 : k_emit_f32, g4, EMIT_WARPS * 32,
-                   emit_smem(logits_dtype), st, true, P);
+                   emit_smem(logits_dtype), st, true, P, 8u);
     if (e == cudaSuccess) e = mark(5);
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

@@ -554,6 +554,7 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
 // w + ACCEPT_WARPS, ...), then warp 0, whose own loads were issued first,
 // decides.
 __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept_all(Params P) {
+    griddep_launch_dependents();
     griddep_wait();  // the row statistics
     const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (b >= P.B) return;
