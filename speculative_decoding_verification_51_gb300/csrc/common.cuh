@@ -6,19 +6,23 @@
 //                (j = 0..n_b) into a row list, zero the counters.
 //   k_row_stats  persistent, one independent bulk-copy pipeline per warp: for
 //                every (valid row, 2048-token chunk) the chunk max, the sum of
-//                exp2((l - max) * log2(e) / T) and (greedy rows) the argmax.
-//                The warp that finishes the last tile of a request then runs
-//                its acceptance (accept.cuh): merge the chunk partials into
-//                per-row (max, Z, argmax), take l(x_j) and q(x_j), draw
-//                Philox uniforms, acceptance bits, first-reject scan (ballot),
-//                write the accepted prefix, queue sampling requests.
-//   k_sample     persistent, warp units: the residual chunk masses of the
+//                exp2((l - max) * log2(e) / T) and (greedy rows) the argmax,
+//                and the gathers l(x_j), q(x_j).  The all-rows pass is
+//                balanced across SMs (each warp's last eighth is claimed by
+//                whichever warp runs out first); an early-exit pass runs the
+//                acceptance of each request it completes (accept.cuh).
+//   k_accept_all one CTA per request (accept.cuh): merge the chunk partials
+//                into per-row (max, Z, argmax), Philox uniforms, acceptance
+//                bits, first-reject scan (ballot), write the accepted prefix,
+//                queue sampling requests.
+//   k_sample     persistent, warp pairs: the residual chunk masses of the
 //                first rejected row of every rejecting request (streaming).
-//   k_emit       one warp per draw: residual tokens (two-level inverse CDF
-//                over the chunk masses) and bonus tokens (over the row-stat
-//                partials).
-// Kernels after k_plan are launched with programmatic dependent launch; each
-// CTA executes griddepcontrol.wait before it touches its predecessor's output.
+//   k_emit       one warp per queue slot: residual tokens (two-level inverse
+//                CDF over the chunk masses) and bonus tokens (over the
+//                row-stat partials).
+// Every kernel executes griddepcontrol.wait before it touches its
+// predecessor's output, so programmatic dependent launch (a build option,
+// off by default: it measured no faster) is safe on any of the launches.
 #pragma once
 
 #include <cuda_runtime.h>
