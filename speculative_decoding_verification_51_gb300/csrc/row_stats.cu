@@ -9,7 +9,9 @@
 // the kernel streams each row from HBM exactly once.
 //
 // Work split: the compacted rows are cut into 2048-token chunks; the
-// (row, chunk) tiles are divided into equal contiguous ranges, one per warp.
+// (row, chunk) tiles are divided into equal contiguous ranges, one per warp
+// (in the all-rows pass a warp streams the first 7/8 of its range and the
+// last eighths go to whichever warps run out first: stream_balanced).
 // Each warp runs its own STATS_STAGES-deep pipeline: lane 0 issues a 1-D bulk
 // copy (cp.async.bulk, completion on a per-stage mbarrier) for the tile
 // STATS_STAGES ahead while the warp reduces the current tile out of shared
@@ -26,8 +28,8 @@
 // No block-wide barrier and no float64 arithmetic (the FP64 pipe of this part
 // is a small fraction of its FP32 rate).  Output: one Partial per tile.
 //
-// Acceptance: after the all-rows pass, k_accept_all (one warp per request)
-// runs every request's acceptance (accept_request).  In an early-exit pass
+// Acceptance: after the all-rows pass, k_accept_all (one CTA per request)
+// runs every request's acceptance (accept_decide).  In an early-exit pass
 // each warp adds the number of tiles it finished for a request to the
 // request's counter (one atomic per contiguous run, after a threadfence) and
 // the warp whose addition completes the row runs the acceptance at once, so
