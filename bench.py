@@ -364,7 +364,9 @@ def run_variant(args, rank, world, local):
     ms = sharding.max_over_ranks(ms, device=dev)
     peak, peak_kind, _ = measured_peak()
     gbs = algo / (ms * 1e-3) / 1e9
-    n_kernels = 3 if args.mode == "tree" else 5  # tree: plan, row stats, walk
+    # tree: plan, row stats, walk; typical: plan, row stats, accept, emit (no
+    # residual draws, so no k_sample)
+    n_kernels = 3 if args.mode == "tree" else 4
     line = {
         "metric": METRIC, "value": world * pos / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),

@@ -243,7 +243,10 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) e = mark(3);
-    if (e == cudaSuccess)
+    // typical acceptance draws every token from p, and without draft
+    // distributions no request can take a residual draw: no k_sample then
+    const bool residuals = rule != RULE_TYPICAL && P.probs != nullptr;
+    if (e == cudaSuccess && residuals)
         e = launch(bf16 ? k_sample_bf16 : k_sample_f32, unsigned(g3), SAMPLE_PAIRS * 64,
                    sample_smem(logits_dtype), st, true, P, 4u);
     if (e == cudaSuccess) e = mark(4);
