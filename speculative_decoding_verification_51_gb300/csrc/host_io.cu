@@ -69,7 +69,9 @@ __global__ void __launch_bounds__(32) k_qx_in(const float* src, float* dst, cons
     }
 }
 
-// grid: one CTA per residual queue slot (after k_accept_all, before k_sample)
+// grid: one CTA per residual queue slot (after k_accept_all, before k_sample).
+// P.probs is the caller's writable d_probs of spec_verify_host (the verifier
+// itself only reads it, hence the const in Params).
 __global__ void __launch_bounds__(HOST_IO_THREADS) k_qrows_in(Params P, const float* src) {
     const int n_res = P.hdr[HDR_NRES];
     for (int slot = blockIdx.x; slot < n_res; slot += gridDim.x) {
