@@ -50,7 +50,6 @@ constexpr int LM_BM = 128, LM_BN = 256, LM_BK = 64, LM_STAGES = 4;
 constexpr int LM_A_BYTES = LM_BM * LM_BK * 2;             // 16 KB
 constexpr int LM_B_BYTES = LM_BN * LM_BK * 2;             // 32 KB
 constexpr int LM_STAGE_BYTES = LM_A_BYTES + LM_B_BYTES;   // 48 KB
-constexpr int LM_B_HALF = LM_B_BYTES / 2;                 // the half one CTA of a pair loads
 constexpr int LM_THREADS = 192;  // warp 0: TMA, warp 1: MMA + TMEM, warps 2..5: epilogue
 constexpr int LM_TMEM_COLS = 2 * LM_BN;
 constexpr uint64_t LM_WAIT_NS = 200000000ull;  // 0.2 s per wait
@@ -87,30 +86,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-// The same box delivered to both CTAs of the pair (same shared-memory offset,
-// completion counted on the barrier at the same offset in each).
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y,
-                                                 uint64_t* bar) {
-    const uint16_t mask = 0x3;
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Every thread of both CTAs of the pair.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -124,17 +99,6 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive on the barrier at the same offset in both CTAs of the pair once this
-// thread's MMAs so far are done.
-__device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
-    const uint16_t mask = 0x3;
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"(mask)
         : "memory");
 }
 
@@ -189,14 +153,10 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // the row tiles of one 2048-column block run side by side, so its slice
     // of the LM head is read from HBM once and then served from L2
-    // Row tiles 2i and 2i+1 form a 2-CTA cluster: each loads half of every
-    // LM-head box and multicasts it to both, so the pair reads it from L2 once.
     const int mt = blockIdx.x, chunk = blockIdx.y;
     const int row0 = mt * LM_BM;
     const int rows = FUSED ? P.hdr[HDR_ROWS] : L.rows;  // fused: the rows k_plan listed
-    if ((mt & ~1) * LM_BM >= rows) return;  // both CTAs of the pair idle: both leave at once
-    const bool idle = row0 >= rows;         // only lends its half of the LM-head boxes
-    const uint32_t crank = cluster_rank();
+    if (row0 >= rows) return;  // a row tile past the list (uniform over the CTA)
     const int col0 = chunk * TILE;
     const int ncols = min(TILE, L.V - col0);
     const int nsub = (ncols + LM_BN - 1) / LM_BN;
@@ -207,7 +167,7 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < LM_STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 2);  // released by the MMAs of both CTAs of the pair
+            mbar_init(&empty[s], 1);  // released by this CTA's MMAs
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&accf[a], 1);
@@ -226,7 +186,6 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();  // both CTAs' barriers exist before either multicasts into them
     tc_fence_after();
     const uint32_t tbase = tmem_base;
     volatile int* abort_v = &abort_flag;
@@ -243,20 +202,18 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                         break;
                     }
                     uint8_t* a = smem + size_t(s) * LM_STAGE_BYTES;
-                    // own A box (not for an idle CTA) + both halves of the B box
-                    mbar_arrive_expect_tx(&full[s],
-                                          (idle ? 0u : uint32_t(LM_A_BYTES)) + uint32_t(LM_B_BYTES));
-                    if (!idle) tma_load_2d(a, &tmA, k * LM_BK, row0, &full[s]);
-                    tma_load_2d_pair(a + LM_A_BYTES + crank * LM_B_HALF, &tmB, k * LM_BK,
-                                     col0 + n * LM_BN + int(crank) * (LM_BN / 2), &full[s]);
+                    // the A box of this row tile and the B box of this sub-tile
+                    mbar_arrive_expect_tx(&full[s], uint32_t(LM_STAGE_BYTES));
+                    tma_load_2d(a, &tmA, k * LM_BK, row0, &full[s]);
+                    tma_load_2d(a + LM_A_BYTES, &tmB, k * LM_BK, col0 + n * LM_BN, &full[s]);
                     if (++s == LM_STAGES) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
             }
-            // every stage released by both CTAs (so every copy has landed and no
-            // arrival is still on its way) before the pair may leave
+            // every stage released (so every copy has landed and no arrival is
+            // still on its way) before the CTA may leave
             for (int k = 0; k < LM_STAGES; ++k) {
                 mbar_wait_bounded(&empty[s], ph ^ 1u, LM_WAIT_NS);
                 if (++s == LM_STAGES) {
@@ -274,8 +231,7 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
             bool issued_any = false;
             for (int n = 0; n < nsub && !*abort_v; ++n) {
                 const int acc = n & 1;
-                if (!idle &&
-                    !mbar_wait_bounded(&acce[acc], (uint32_t(n >> 1) & 1u) ^ 1u, LM_WAIT_NS)) {
+                if (!mbar_wait_bounded(&acce[acc], (uint32_t(n >> 1) & 1u) ^ 1u, LM_WAIT_NS)) {
                     *abort_v = 1;
                     break;
                 }
@@ -289,29 +245,27 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                     tc_fence_after();
                     const uint32_t a = smem_u32(smem + size_t(s) * LM_STAGE_BYTES);
                     const uint32_t b = a + LM_A_BYTES;
-                    if (!idle) {
 #pragma unroll
-                        for (int kk = 0; kk < LM_BK / 16; ++kk)
-                            tc_mma(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
-                                   (k > 0 || kk > 0) ? 1u : 0u);
-                        issued_any = true;
-                    }
-                    // the stage is free, in both CTAs, once these MMAs are done
-                    tc_commit_pair(&empty[s]);
+                    for (int kk = 0; kk < LM_BK / 16; ++kk)
+                        tc_mma(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
+                               (k > 0 || kk > 0) ? 1u : 0u);
+                    issued_any = true;
+                    // the stage is free once these MMAs are done
+                    tc_commit(&empty[s]);
                     if (++s == LM_STAGES) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
                 if (*abort_v) break;
-                if (!idle) tc_commit(&accf[acc]);  // the sub-tile's accumulator is complete
+                tc_commit(&accf[acc]);  // the sub-tile's accumulator is complete
             }
             if (issued_any) {  // every MMA of this CTA is done before TMEM is freed
                 tc_commit(&fin);
                 mbar_wait_bounded(&fin, 0, LM_WAIT_NS);
             }
         }
-    } else if (!idle) {
+    } else {
         // ---- epilogue: TMEM -> registers -> bf16 logits, one row per thread
         const int q = warp & 3;  // the TMEM lane quarter this warp may read
         const int r = row0 + q * 32 + lane;
@@ -433,7 +387,6 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
-    cluster_sync();  // the peer has finished with this CTA's shared memory
     tc_fence_after();
     if (warp == 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),
@@ -495,26 +448,14 @@ spec_status make_map(CUtensorMap* map, const void* base, int rows, int H, int bo
     return r == CUDA_SUCCESS ? SPEC_OK : SPEC_ERR_INVALID_ARG;
 }
 
-// Row tiles of `rows`, rounded up to whole 2-CTA clusters.
-int pair_tiles(int rows) { return ((rows + 2 * LM_BM - 1) / (2 * LM_BM)) * 2; }
+// Row tiles of `rows`.
+int row_tiles(int rows) { return (rows + LM_BM - 1) / LM_BM; }
 
-// k_lmhead in 2-CTA clusters along the row tiles.
 template <bool FUSED>
 cudaError_t launch_lm(dim3 grid, cudaStream_t st, const CUtensorMap& ma, const CUtensorMap& mb,
                       const LmArgs& L, const Params& P) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(LM_THREADS);
-    cfg.dynamicSmemBytes = LM_SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 2;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_lmhead<FUSED>, ma, mb, L, P);
+    k_lmhead<FUSED><<<grid, LM_THREADS, LM_SMEM, st>>>(ma, mb, L, P);
+    return cudaGetLastError();
 }
 
 // Per-device kernel attributes (shared memory above 48 KB), set once.
@@ -545,7 +486,7 @@ spec_status launch_lmhead_fused(const Params& P, const LmHeadIn& in, cudaStream_
     CUtensorMap ma, mb;
     spec_status r = make_map(&ma, in.hid_c, maxrows, in.H, LM_BM);
     if (r != SPEC_OK) return r;
-    r = make_map(&mb, in.lm_head, P.V, in.H, LM_BN / 2);  // each CTA of a pair loads half a box
+    r = make_map(&mb, in.lm_head, P.V, in.H, LM_BN);
     if (r != SPEC_OK) return r;
     if (lm_prepare() != SPEC_OK) return SPEC_ERR_CUDA;
     const int gblocks = min((maxrows + 7) / 8, 4096);
@@ -556,7 +497,7 @@ spec_status launch_lmhead_fused(const Params& P, const LmHeadIn& in, cudaStream_
     L.V = P.V;
     L.out = static_cast<uint16_t*>(const_cast<void*>(P.logits));
     L.status = P.status;
-    const dim3 grid(unsigned(pair_tiles(maxrows)), unsigned(P.C));
+    const dim3 grid(unsigned(row_tiles(maxrows)), unsigned(P.C));
     if (launch_lm<true>(grid, st, ma, mb, L, P) != cudaSuccess) return SPEC_ERR_CUDA;
     k_accept_all<<<P.B, ACCEPT_WARPS * 32, 0, st>>>(P);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
@@ -579,7 +520,7 @@ spec_status spec_lmhead_logits(const void* hidden, const void* lm_head, int rows
     CUtensorMap ma, mb;
     spec_status st = make_map(&ma, hidden, rows, H, LM_BM);
     if (st != SPEC_OK) return st;
-    st = make_map(&mb, lm_head, V, H, LM_BN / 2);  // each CTA of a pair loads half a box
+    st = make_map(&mb, lm_head, V, H, LM_BN);
     if (st != SPEC_OK) return st;
     if (lm_prepare() != SPEC_OK) return SPEC_ERR_CUDA;
     LmArgs L;
@@ -589,7 +530,7 @@ spec_status spec_lmhead_logits(const void* hidden, const void* lm_head, int rows
     L.out = static_cast<uint16_t*>(logits_out);
     L.status = dev_status;
     Params P = {};
-    const dim3 grid(unsigned(pair_tiles(rows)), unsigned((V + TILE - 1) / TILE));
+    const dim3 grid(unsigned(row_tiles(rows)), unsigned((V + TILE - 1) / TILE));
     if (launch_lm<false>(grid, reinterpret_cast<cudaStream_t>(stream), ma, mb, L, P) !=
         cudaSuccess)
         return SPEC_ERR_CUDA;
