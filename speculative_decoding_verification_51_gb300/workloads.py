@@ -29,6 +29,7 @@ positions j >= num_draft[b] are set to -1: the verifier must never read them.
 """
 from __future__ import annotations
 
+import functools
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -98,86 +99,128 @@ class Workload:
         return self.subset(list(range(B)))
 
 
-def _zipf_logits(B, K1, V, g, device):
+def _zipf_logits(nb, K1, V, g):
     """-1.1 ln(rank) placed by one permutation per request, + N(0, 1) noise."""
-    rank = torch.arange(1, V + 1, device=device, dtype=torch.float32)
+    rank = torch.arange(1, V + 1, dtype=torch.float32)
     base = -1.1 * torch.log(rank)                                   # [V]
-    perm = torch.argsort(torch.rand(B, V, generator=g, device=device), dim=1)
-    placed = torch.empty(B, V, device=device, dtype=torch.float32)
-    placed.scatter_(1, perm, base.expand(B, V).contiguous())        # token perm[r] gets rank r
-    noise = torch.randn(B, K1, V, generator=g, device=device)
+    perm = torch.argsort(torch.rand(nb, V, generator=g), dim=1)
+    placed = torch.empty(nb, V, dtype=torch.float32)
+    placed.scatter_(1, perm, base.expand(nb, V).contiguous())       # token perm[r] gets rank r
+    noise = torch.randn(nb, K1, V, generator=g)
     return placed[:, None, :] + noise
+
+
+# requests generated together (bounds the host memory of the largest workloads)
+GEN_BLOCK = 32
+
+
+def _draw(q: torch.Tensor, g: torch.Generator) -> torch.Tensor:
+    """One token per row of q [R, V] (rows summing to about 1): the first
+    token whose float64 running sum exceeds u * (row total), u ~ U[0, 1).
+    A token of zero mass is never drawn."""
+    cdf = torch.cumsum(q.to(torch.float64), dim=-1)
+    u = torch.rand(q.shape[0], generator=g, dtype=torch.float64)
+    t = (u * cdf[:, -1]).unsqueeze(1)
+    x = torch.searchsorted(cdf, t, right=True).squeeze(1)
+    return x.clamp_(max=q.shape[1] - 1)
 
 
 def make_workload(cid: int, device="cpu", *, gen_seed: int | None = None, B: int | None = None,
                   K: int | None = None, V: int | None = None) -> Workload:
-    """Build workload ``cid`` (1..5) on ``device`` from a seeded generator.
+    """Build workload ``cid`` (1..5) from a seeded CPU generator, then copy it
+    to ``device``: a named workload is one fixed set of inputs on every device.
 
+    The per-request scalars (draft counts, temperatures, draft noise) are drawn
+    first for the whole batch, then the rows request block by request block
+    (GEN_BLOCK requests at a time), all from one generator stream.
     B, K, V override the sizes (for small parity cases of the same recipe).
+    The host tensors of the last few workloads built are kept, so a repeated
+    build only copies; every call returns tensors of its own.
     """
     spec = SPECS[cid]
     B = spec.B if B is None else B
     K = spec.K if K is None else K
     V = spec.V if V is None else V
     seed = 1000 + cid if gen_seed is None else gen_seed
-    g = torch.Generator(device=device)
+    t = _generate(cid, seed, B, K, V)
+    logits, probs, ids, num, temp = (x.to(device, copy=True) for x in t[:5])
+    return Workload(spec, logits, probs, ids, num, temp, VERIFY_SEED,
+                    {"gen_seed": seed, "draft_noise": t[5]})
+
+
+@functools.lru_cache(maxsize=3)
+def _generate(cid: int, seed: int, B: int, K: int, V: int):
+    """Host tensors (logits, draft_probs, draft_ids, num_draft, temperature,
+    draft noise list or None) of workload ``cid`` at these sizes."""
+    spec = SPECS[cid]
+    g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     K1 = K + 1
     f32 = torch.float32
 
+    # ---- per-request scalars
     if cid == 1:
-        target = 2.0 * torch.randn(B, K1, V, generator=g, device=device)
-        draft_noise = torch.ones(B, device=device)
-        num_draft = torch.full((B,), K, dtype=torch.int32, device=device)
-        temp = torch.ones(B, device=device)
+        draft_noise = torch.ones(B)
+        num_draft = torch.full((B,), K, dtype=torch.int32)
+        temp = torch.ones(B)
     elif cid == 2:
-        target = 3.0 * torch.randn(B, K1, V, generator=g, device=device)
-        boost = torch.randint(0, V, (B, K1, 1), generator=g, device=device)
-        target.scatter_add_(2, boost, torch.full((B, K1, 1), 8.0, device=device))
-        draft_noise = torch.full((B,), 1.5, device=device)
-        num_draft = torch.full((B,), K, dtype=torch.int32, device=device)
-        temp = torch.ones(B, device=device)
+        draft_noise = torch.full((B,), 1.5)
+        num_draft = torch.full((B,), K, dtype=torch.int32)
+        temp = torch.ones(B)
         temp[1::2] = 0.0  # odd requests greedy
-    elif cid in (3, 4, 5):
-        target = _zipf_logits(B, K1, V, g, device)
-        if cid == 3:
-            draft_noise = torch.ones(B, device=device)
-            num_draft = torch.full((B,), K, dtype=torch.int32, device=device)
-            temp = 0.5 + 0.7 * torch.rand(B, generator=g, device=device)
-        elif cid == 4:
-            sig = torch.tensor([0.25, 1.0, 4.0], device=device)
-            draft_noise = sig[torch.randint(0, 3, (B,), generator=g, device=device)]
-            num_draft = torch.randint(0, K + 1, (B,), generator=g, device=device).to(torch.int32)
-            temp = 0.5 + 0.7 * torch.rand(B, generator=g, device=device)
-            greedy = torch.rand(B, generator=g, device=device) < 0.25
-            temp = torch.where(greedy, torch.zeros_like(temp), temp)
-        else:
-            draft_noise = torch.full((B,), 0.5, device=device)
-            num_draft = torch.randint(1, K + 1, (B,), generator=g, device=device).to(torch.int32)
-            temp = 0.3 + 1.2 * torch.rand(B, generator=g, device=device)
+    elif cid == 3:
+        draft_noise = torch.ones(B)
+        num_draft = torch.full((B,), K, dtype=torch.int32)
+        temp = 0.5 + 0.7 * torch.rand(B, generator=g)
+    elif cid == 4:
+        sig = torch.tensor([0.25, 1.0, 4.0])
+        draft_noise = sig[torch.randint(0, 3, (B,), generator=g)]
+        num_draft = torch.randint(0, K + 1, (B,), generator=g).to(torch.int32)
+        temp = 0.5 + 0.7 * torch.rand(B, generator=g)
+        greedy = torch.rand(B, generator=g) < 0.25
+        temp = torch.where(greedy, torch.zeros_like(temp), temp)
+    elif cid == 5:
+        draft_noise = torch.full((B,), 0.5)
+        num_draft = torch.randint(1, K + 1, (B,), generator=g).to(torch.int32)
+        temp = 0.3 + 1.2 * torch.rand(B, generator=g)
     else:
         raise ValueError(f"unknown workload {cid}")
+    temp = temp.to(f32)
 
-    # the simulated drafter sees the first K rows of the target plus noise
-    dlog = target[:, :K, :] + draft_noise[:, None, None] * torch.randn(
-        B, K, V, generator=g, device=device)
-    t_draft = torch.where(temp > 0, temp, torch.ones_like(temp))
-    draft_probs = torch.softmax(dlog / t_draft[:, None, None], dim=-1).to(f32).contiguous()
-    if K > 0:
-        sampled = torch.multinomial(draft_probs.reshape(B * K, V), 1, generator=g).reshape(B, K)
-        greedy_ids = dlog.argmax(dim=-1)
-        draft_ids = torch.where((temp > 0)[:, None], sampled, greedy_ids).to(torch.int32)
-        pos = torch.arange(K, device=device)[None, :]
-        draft_ids = torch.where(pos < num_draft[:, None].long(), draft_ids,
-                                torch.full_like(draft_ids, -1)).contiguous()
-    else:
-        draft_ids = torch.empty(B, 0, dtype=torch.int32, device=device)
+    ldt = torch.bfloat16 if spec.dtype == "bf16" else f32
+    logits = torch.empty((B, K1, V), dtype=ldt)
+    draft_probs = torch.empty((B, K, V), dtype=f32)
+    draft_ids = torch.full((B, K), -1, dtype=torch.int32)
+    for b0 in range(0, B, GEN_BLOCK):
+        b1 = min(B, b0 + GEN_BLOCK)
+        nb = b1 - b0
+        if cid == 1:
+            target = 2.0 * torch.randn(nb, K1, V, generator=g)
+        elif cid == 2:
+            target = 3.0 * torch.randn(nb, K1, V, generator=g)
+            boost = torch.randint(0, V, (nb, K1, 1), generator=g)
+            target.scatter_add_(2, boost, torch.full((nb, K1, 1), 8.0))
+        else:
+            target = _zipf_logits(nb, K1, V, g)
+        # the simulated drafter sees the first K rows of the target plus noise
+        dlog = target[:, :K, :] + draft_noise[b0:b1, None, None] * torch.randn(
+            nb, K, V, generator=g)
+        tb = temp[b0:b1]
+        t_draft = torch.where(tb > 0, tb, torch.ones_like(tb))
+        q = torch.softmax(dlog / t_draft[:, None, None], dim=-1).to(f32).contiguous()
+        if K > 0:
+            sampled = _draw(q.reshape(nb * K, V), g).reshape(nb, K)
+            greedy_ids = dlog.argmax(dim=-1)
+            ids = torch.where((tb > 0)[:, None], sampled, greedy_ids).to(torch.int32)
+            pos = torch.arange(K)[None, :]
+            draft_ids[b0:b1] = torch.where(pos < num_draft[b0:b1, None].long(), ids,
+                                           torch.full_like(ids, -1))
+        logits[b0:b1] = target.to(ldt)
+        draft_probs[b0:b1] = q
+        del target, dlog, q
 
-    logits = target.to(torch.bfloat16 if spec.dtype == "bf16" else f32).contiguous()
-    return Workload(spec, logits, draft_probs, draft_ids, num_draft.contiguous(),
-                    temp.to(f32).contiguous(), VERIFY_SEED,
-                    {"gen_seed": seed, "draft_noise": draft_noise.cpu().tolist()
-                     if B <= 16 else None})
+    return (logits, draft_probs, draft_ids.contiguous(), num_draft.contiguous(),
+            temp.contiguous(), draft_noise.tolist() if B <= 16 else None)
 
 
 def to_numpy(w: Workload) -> dict:

@@ -48,3 +48,25 @@ def test_config2_half_greedy_and_oracle_runs():
 def test_counts():
     nd = torch.tensor([0, 3, 1])
     assert W.valid_rows(nd) == 7 and W.positions(nd) == 4
+
+
+def test_named_workload_is_one_input_set():
+    """The generator runs on the host whatever the target device, so a named
+    workload is the same inputs everywhere; repeated builds return their own
+    tensors (the host cache hands out copies)."""
+    a = W.make_workload(3, B=8, V=2048)
+    b = W.make_workload(3, B=8, V=2048)
+    assert a.target_logits.data_ptr() != b.target_logits.data_ptr()
+    a.target_logits.zero_()
+    c = W.make_workload(3, B=8, V=2048)
+    assert torch.equal(b.target_logits, c.target_logits)
+    assert not torch.equal(a.target_logits, c.target_logits)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cid", [2, 4])
+def test_device_copy_equals_host_build(cid):
+    h = W.make_workload(cid, device="cpu")
+    d = W.make_workload(cid, device="cuda")
+    for k in ("target_logits", "draft_probs", "draft_ids", "num_draft", "temperature"):
+        assert torch.equal(getattr(h, k), getattr(d, k).cpu()), k
