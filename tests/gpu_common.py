@@ -50,6 +50,13 @@ def check_parity(w: W.Workload, tag: str, **kw) -> parity.Report:
     return rep
 
 
+def assert_excused_within_bound(rep: parity.Report) -> None:
+    """Near-tie decisions that differ from the oracle (counted as excused)
+    must stay under 1e-4 of the rows of the batch: zero at the sizes of the
+    measured workloads."""
+    assert rep.excused < 1e-4 * rep.rows, rep.summary()
+
+
 def run_gpu_typical(w: W.Workload, threshold: float, debug=True, **kw):
     ensure_built()
     res = binding.spec_verify_typical(w.target_logits, w.draft_ids, w.num_draft, w.temperature,

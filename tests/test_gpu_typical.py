@@ -9,7 +9,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_common import check_parity_typical, custom_workload, run_gpu_typical
+from gpu_common import (assert_excused_within_bound, check_parity_typical, custom_workload,
+                        run_gpu_typical)
 from speculative_decoding_verification_51_gb300 import binding
 from speculative_decoding_verification_51_gb300 import workloads as W
 
@@ -19,7 +20,7 @@ pytestmark = pytest.mark.gpu
 def _assert_ok(rep):
     assert not rep.failures, rep.failures[:5]
     assert rep.max_p_rel <= 1e-5
-    assert rep.excused <= max(1, 0.01 * rep.sampling), rep.summary()
+    assert_excused_within_bound(rep)
 
 
 @pytest.mark.parametrize("cid,theta", [(1, 1e-3), (1, 0.02), (2, 1e-3), (2, 0.05),

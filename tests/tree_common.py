@@ -25,6 +25,7 @@ TIE = 1e-6
 @dataclass
 class TreeReport:
     requests: int = 0
+    rows: int = 0  # node rows of the batch (B x N)
     greedy: int = 0
     sampling: int = 0
     bad: int = 0
@@ -46,7 +47,7 @@ class TreeReport:
 def compare_tree(inp: dict, ids, nacc, last, dbg, ref: dict, req_index=None) -> TreeReport:
     T = inp["temperature"]
     B = T.shape[0]
-    rep = TreeReport(requests=B)
+    rep = TreeReport(requests=B, rows=int(np.asarray(inp["tree_tokens"]).size))
     probe = []
     for b in range(B):
         ao = int(ref["out_num_accepted"][b])
