@@ -61,6 +61,10 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--oracle-seconds", type=float, default=1.0,
+                    help="budget of each per-config oracle timing (1 thread, all cores)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config table (every workload and config 5's B sweep)")
     ap.add_argument("--mode", choices=["chain", "typical", "tree", "early_exit", "lmhead"], default="chain",
                     help="chain: the lossless / greedy verifier (the headline line); "
                          "typical: typical acceptance on the same workload; tree: "
@@ -91,24 +95,24 @@ def measured_peak():
         return PEAK_FALLBACK_GBS, "fallback", {}
 
 
-def row_stats_sha():
-    """Digest of the sources k_row_stats is compiled from."""
+def verify_sha():
+    """Digest of the sources k_verify is compiled from."""
     h = hashlib.sha256()
-    for f in ("row_stats.cu", "accept.cuh", "common.cuh"):
+    for f in ("verify.cu", "stats.cuh", "draw.cuh", "accept.cuh", "common.cuh"):
         h.update(open(os.path.join(ROOT, "speculative_decoding_verification_51_gb300", "csrc", f),
                       "rb").read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload_name: str):
-    """ncu DRAM bytes per launch of k_row_stats for this workload, if the
+    """ncu DRAM bytes per launch of k_verify for this workload, if the
     committed summary was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "row_stats_traffic.json")
+    p = os.path.join(ROOT, "profiles", "verify_traffic.json")
     try:
         d = json.load(open(p))
     except Exception:
         return None
-    if d.get("source_sha") != row_stats_sha():
+    if d.get("source_sha") != verify_sha():
         return None
     e = d.get("workloads", {}).get(workload_name)
     return None if e is None else float(e["dram_bytes_per_launch"])
@@ -208,25 +212,6 @@ class ClockSampler:
 
 def workload_name(cid, B):
     return f"config{cid}" + (f"_B{B}" if B else "")
-
-
-def algorithmic_bytes(w, nacc_mode=None):
-    """(row_stats bytes per launch, whole-step algorithmic bytes)."""
-    n = w.num_draft.long().cpu()
-    V, esz = w.V, (2 if w.target_logits.dtype == torch.bfloat16 else 4)
-    rows = int((n + 1).sum())
-    C = (V + TILE - 1) // TILE
-    stats = rows * V * esz + rows * C * 16
-    step = rows * V * esz
-    if nacc_mode is not None:
-        a, greedy = nacc_mode
-        T = w.temperature.cpu()
-        sampling = T > 0
-        resid = int(((a < n) & sampling).sum())
-        step += resid * V * 4                              # q row at the first rejection
-        step += int(n[sampling].sum()) * 4                 # q(x_j) gathers
-    step += w.B * (w.K * 4 + 4 + 4) + w.B * ((w.K + 1) * 4 + 4)  # ids, n, T in; outputs
-    return stats, step
 
 
 def run_reference(args, rank, world):
@@ -651,8 +636,173 @@ def main():
         run_variant(args, rank, world, local)
         return
 
+    run_chain(args, rank, world, local)
+
+
+
+# ---------------------------------------------------------------- chain mode
+
+SWEEP = ((5, 32), (5, 128))  # config 5's B sweep (B = 512 is config 5 itself)
+
+
+def call_bytes(w, nacc_log):
+    """Bytes per call, averaged over the calls whose a_b are in nacc_log
+    [calls, B]: 'algorithmic' = every valid logits row 0..n_b once + the q row
+    of each residual draw + the q(x_j) gathers + ids, counts, temperatures and
+    outputs; 'literal' = logits + draft probabilities once (rows 0..n_b and
+    q rows 0..n_b-1); 'read' = what a verifier that stops at the first
+    rejection must read: rows 0..a_b, the residual q rows, the same small
+    terms."""
+    n = w.num_draft.long().cpu()
+    T = w.temperature.cpu()
+    V, esz = w.V, (2 if w.target_logits.dtype == torch.bfloat16 else 4)
+    ok = (n >= 0) & (n <= w.K)
+    samp = (T > 0) & ok
+    nl = nacc_log.long()
+    valid = nl >= 0
+    resid = ((nl < n[None]) & valid & samp[None]).sum(1).double().mean().item()
+    rows_read = ((nl + 1) * valid).sum(1).double().mean().item()
+    small = w.B * (w.K * 4 + 8) + w.B * ((w.K + 1) * 4 + 4) + int(n[samp].sum()) * 4
+    rows_all = int(((n + 1) * ok).sum())
+    return {"algorithmic": rows_all * V * esz + resid * V * 4 + small,
+            "literal": rows_all * V * esz + int((n * ok).sum()) * V * 4,
+            "read": rows_read * V * esz + resid * V * 4 + small,
+            "rows_all": rows_all, "rows_read": rows_read, "residual_rows": resid}
+
+
+class Caller:
+    """One verification call on a workload, captured in a CUDA graph with the
+    seed read from device memory (a step writes its seed, then replays)."""
+
+    def __init__(self, w, dev, offset, all_rows=False):
+        from speculative_decoding_verification_51_gb300 import binding
+        self.w, self.dev, self.binding = w, dev, binding
+        B, K, V = w.B, w.K, w.V
+        self.ws = binding.new_workspace(B, K, V, dev)
+        self.out_ids = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+        self.out_nacc = torch.empty((B,), dtype=torch.int32, device=dev)
+        self.seed_buf = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.offset, self.all_rows = offset, all_rows
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap):
+            self._call(cap)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=cap):
+            self._call(cap)
+        torch.cuda.synchronize()
+
+    def _call(self, st):
+        w = self.w
+        self.binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
+                                 w.temperature, 0, out_ids=self.out_ids,
+                                 out_num_accepted=self.out_nacc, workspace=self.ws,
+                                 request_offset=self.offset, seed_dev=self.seed_buf, stream=st,
+                                 all_rows=self.all_rows)
+
+    def direct(self, seed):
+        w = self.w
+        self.binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
+                                 w.temperature, seed, out_ids=self.out_ids,
+                                 out_num_accepted=self.out_nacc, workspace=self.ws,
+                                 request_offset=self.offset, all_rows=self.all_rows)
+
+
+class L2Flush:
+    """Write 256 MiB, then read another 256 MiB: the L2 ends up full of clean
+    lines of unrelated data, so the timed call neither hits its own inputs in
+    L2 nor pays for write-backs it did not cause."""
+
+    def __init__(self, dev):
+        self.a = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.b = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self, i):
+        self.a.fill_(i & 0xFF)
+        self.b.sum()
+
+
+def time_replays(c, steps, stream, flush=None, seed0=2000):
+    """Device time (ms) of each of `steps` graph replays, L2 flushed before
+    each when `flush` is given; the a_b of every replay are kept."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    nacc_log = torch.empty((steps, c.w.B), dtype=torch.int32, device=c.dev)
+    for i in range(steps):
+        if flush is not None:
+            flush(i + 7)
+        c.seed_buf.fill_(seed0 + i)
+        evs[i][0].record(stream)
+        c.graph.replay()
+        evs[i][1].record(stream)
+        nacc_log[i].copy_(c.out_nacc)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs], nacc_log.cpu()
+
+
+def oracle_rate(w, threads, budget_s):
+    """The float64 oracle (as it stands) on a bounded leading sample of the
+    workload's requests: (positions/s, the sample, threads used)."""
+    import oracle
+    from speculative_decoding_verification_51_gb300 import workloads as W
+    inputs = W.to_numpy(w)
+    B = w.B
+    nb, t = 1, 0.0
+    while True:  # grow the sample until one pass takes about a quarter of the budget
+        sub = {k: (v[:nb] if isinstance(v, np.ndarray) else v) for k, v in inputs.items()}
+        t0 = time.perf_counter()
+        oracle.spec_verify(**sub, n_threads=threads)
+        t = time.perf_counter() - t0
+        if nb == B or t >= budget_s / 4:
+            break
+        nb = min(B, nb * 4)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.spec_verify(**sub, n_threads=threads)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s or reps >= 200:
+            break
+    sec = (time.perf_counter() - t0) / reps
+    pos = int(np.clip(sub["num_draft"], 0, None).sum())
+    return pos / sec, f"{nb} of {B} requests ({pos} positions) x {reps}, {sec * 1e3:.2f} ms each"
+
+
+def measure_config(w, dev, offset, steps, stream, flush, peak):
+    """Cold- and hot-L2 time per call of one workload, with its byte figures."""
+    from speculative_decoding_verification_51_gb300 import workloads as W
+    c = Caller(w, dev, offset)
+    for i in range(3):
+        flush(i)
+        c.seed_buf.fill_(1500 + i)
+        c.graph.replay()
+    torch.cuda.synchronize()
+    cold, nacc_log = time_replays(c, steps, stream, flush)
+    hot, _ = time_replays(c, steps, stream, None, seed0=2000)
+    ms_cold, ms_hot = statistics.mean(cold), statistics.mean(hot)
+    by = call_bytes(w, nacc_log)
+    pos = W.positions(w.num_draft)
+    valid = nacc_log >= 0
+    acc = float((nacc_log.clamp(min=0)).sum()) / max(1, pos * nacc_log.shape[0])
+    out = {"B": w.B, "K": w.K, "V": w.V, "positions_per_call": pos,
+           "ms_per_call_cold_l2": round(ms_cold, 5), "ms_per_call_hot_l2": round(ms_hot, 5),
+           "positions_per_s": round(pos / (ms_cold * 1e-3), 1),
+           "accept_rate": round(acc, 4), "rows_all": by["rows_all"],
+           "rows_read": round(by["rows_read"], 1), "residual_rows": round(by["residual_rows"], 1)}
+    for k in ("algorithmic", "literal", "read"):
+        gbs = by[k] / (ms_cold * 1e-3) / 1e9
+        out[f"{k}_bytes"] = int(by[k])
+        out[f"{k}_gbs"] = round(gbs, 1)
+        out[f"{k}_frac"] = round(gbs / peak, 4)
+    out["requests_all_valid"] = bool(valid.all())
+    del c
+    return out
+
+
+def run_chain(args, rank, world, local):
     from speculative_decoding_verification_51_gb300 import binding
     from speculative_decoding_verification_51_gb300 import build as _build
+    from speculative_decoding_verification_51_gb300 import sharding
     from speculative_decoding_verification_51_gb300 import workloads as W
 
     torch.cuda.set_device(local)
@@ -662,183 +812,125 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     _build.build()
     binding.lib()
+    peak, peak_kind, _ = measured_peak()
+    stream = torch.cuda.current_stream(dev)
+    flush = L2Flush(dev)
 
-    from speculative_decoding_verification_51_gb300 import sharding
     w = W.make_workload(args.config, device=dev)
     if args.batch:
         w = w.leading(args.batch)
     B, K, V = w.B, w.K, w.V
     offset = sharding.weak_offset(rank, B)  # each rank holds its own requests
     pos = W.positions(w.num_draft)
-    ws = binding.new_workspace(B, K, V, dev)
-    out_ids = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
-    out_nacc = torch.empty((B,), dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def flush_l2(i):
-        """Write 256 MiB, then read another 256 MiB: the L2 ends up full of
-        clean lines of unrelated data, so the timed call neither hits its own
-        inputs in L2 nor pays for write-backs it did not cause."""
-        flush.fill_(i & 0xFF)
-        flush_rd.sum()
-
-    def step(seed):
-        if offset:
-            binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
-                                w.temperature, seed, out_ids=out_ids, out_num_accepted=out_nacc,
-                                workspace=ws, request_offset=offset)
-        else:
-            binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
-                                w.temperature, seed, out_ids=out_ids, out_num_accepted=out_nacc,
-                                workspace=ws)
-
+    c = Caller(w, dev, offset)
     for i in range(args.warmup):
-        flush_l2(i)
-        step(1000 + i)
-    torch.cuda.synchronize()
-
-    # One call captured in a CUDA graph, the seed read from device memory: a
-    # step writes its seed, then replays the four kernels of the call.
-    seed_buf = torch.zeros(1, dtype=torch.int64, device=dev)
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    with torch.cuda.stream(cap):
-        binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
-                            w.temperature, 0, out_ids=out_ids, out_num_accepted=out_nacc,
-                            workspace=ws, request_offset=offset, seed_dev=seed_buf, stream=cap)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=cap):
-        binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
-                            w.temperature, 0, out_ids=out_ids, out_num_accepted=out_nacc,
-                            workspace=ws, request_offset=offset, seed_dev=seed_buf, stream=cap)
-    torch.cuda.synchronize()
+        flush(i)
+        c.direct(1000 + i)
     for i in range(args.warmup):
-        flush_l2(i)
-        seed_buf.fill_(1500 + i)
-        graph.replay()
+        flush(i)
+        c.seed_buf.fill_(1500 + i)
+        c.graph.replay()
     torch.cuda.synchronize()
 
     # ---- timed region: K steps, device time per step, L2 flushed before each
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev) as clk:
-        for i in range(args.steps):
-            flush_l2(i + 7)
-            seed_buf.fill_(2000 + i)
-            evs[i][0].record(stream)
-            graph.replay()
-            evs[i][1].record(stream)
-        torch.cuda.synchronize()
+        step_ms, nacc_log = time_replays(c, args.steps, stream, flush)
     if world > 1:
         torch.distributed.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in evs]
-    ms = sum(step_ms) / len(step_ms)
-    ms = sharding.max_over_ranks(ms, device=dev)
+    ms = sharding.max_over_ranks(sum(step_ms) / len(step_ms), device=dev)
     clocks = clk.summary()
 
-    # the same calls launched directly (no graph), for comparison
-    n_direct = min(args.steps, 50)
+    # the same call launched directly (no graph), and the all-rows verifier
+    n_aux = min(args.steps, 50)
     devs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(n_direct)]
-    torch.cuda.synchronize()
-    for i in range(n_direct):
-        flush_l2(i + 5)
+            for _ in range(n_aux)]
+    for i in range(n_aux):
+        flush(i + 5)
         devs[i][0].record(stream)
-        step(2500 + i)
+        c.direct(2500 + i)
         devs[i][1].record(stream)
     torch.cuda.synchronize()
     ms_direct = statistics.mean(a.elapsed_time(b) for a, b in devs)
+    ca = Caller(w, dev, offset, all_rows=True)
+    for i in range(3):
+        flush(i)
+        ca.graph.replay()
+    torch.cuda.synchronize()
+    ms_all_rows = statistics.mean(time_replays(ca, n_aux, stream, flush)[0])
+    del ca
 
-    # ---- per-kernel durations (same workload, marks between the kernels)
-    n_prof = min(args.steps, 50)
-    nk = binding.N_KERNELS
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(n_prof)]
+    # ---- per-kernel durations (marks between the kernels of the call)
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(binding.N_MARKS)]
+             for _ in range(n_aux)]
     for m in marks:
         for e in m:
             e.record(stream)
     torch.cuda.synchronize()
-    for i in range(n_prof):
-        flush_l2(i + 3)
+    for i in range(n_aux):
+        flush(i + 3)
         binding.spec_verify_profiled(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
-                                     w.temperature, 3000 + i, out_ids, out_nacc, ws, marks[i])
+                                     w.temperature, 3000 + i, c.out_ids, c.out_nacc, c.ws,
+                                     marks[i])
     torch.cuda.synchronize()
-    kern_ms = [statistics.mean(m[k].elapsed_time(m[k + 1]) for m in marks) for k in range(nk)]
-    names = list(binding.KERNELS)
+    kern_ms = [statistics.mean(m[k].elapsed_time(m[k + 1]) for m in marks)
+               for k in range(binding.N_KERNELS)]
 
-    # ---- algorithmic bytes
-    nacc_cpu = out_nacc.cpu().long()
-    stats_bytes, step_bytes = algorithmic_bytes(w, (nacc_cpu, None))
-    peak, peak_kind, _ = measured_peak()
-    ach = stats_bytes / (kern_ms[1] * 1e-3) / 1e9
+    # ---- bytes and the roofline of k_verify (the whole verification)
+    by = call_bytes(w, nacc_log)
+    t_kern = kern_ms[1]
+    ach = by["read"] / (t_kern * 1e-3) / 1e9
     wname = workload_name(args.config, args.batch)
     roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "traffic": profiled_traffic(wname),
-                "kernel": "k_row_stats", "kernel_ms": round(kern_ms[1], 5),
-                "algorithmic_bytes_per_launch": stats_bytes, "peak_kind": peak_kind}
+                "kernel": "k_verify", "kernel_ms": round(t_kern, 5),
+                "algorithmic_bytes_per_launch": int(by["read"]),
+                "bytes_definition": "rows 0..a_b of every request + the q row of each "
+                                    "residual draw + gathers, ids, counts and outputs",
+                "peak_kind": peak_kind}
+    gate_gbs = by["algorithmic"] / (ms * 1e-3) / 1e9
+    literal_gbs = by["literal"] / (ms * 1e-3) / 1e9
 
-    # ---- end to end through host buffers
+    # ---- end to end through host buffers (spec_verify_host)
     e2e = None
     if not args.no_e2e:
-        h = {k: getattr(w, k).cpu().pin_memory() for k in
-             ("target_logits", "draft_probs", "draft_ids", "num_draft", "temperature")}
-        h_out = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
-        h_nacc = torch.empty((B,), dtype=torch.int32).pin_memory()
-        d_l = torch.empty_like(w.target_logits)
-        d_p = torch.empty_like(w.draft_probs)
-        small = torch.empty(binding.host_small_bytes(B, K), dtype=torch.uint8, device=dev)
-        e2e_steps = max(3, min(args.steps, 10))
+        e2e = e2e_host(w, dev, stream, args, world, pos)
 
-        def host_step(seed):
-            binding.spec_verify_host(h["target_logits"], h["draft_probs"], h["draft_ids"],
-                                     h["num_draft"], h["temperature"], seed, h_out, h_nacc, d_l,
-                                     d_p, small, ws)
-
-        for i in range(2):
-            host_step(4000 + i)
-        torch.cuda.synchronize()
-        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a_ev.record(stream)
-        for i in range(e2e_steps):
-            host_step(5000 + i)
-        b_ev.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = a_ev.elapsed_time(b_ev) / e2e_steps
-        # Pinned (mapped) host buffers take the rows-only path of
-        # spec_verify_host: the logits rows 0..n_b, q_j(x_j) of every draft,
-        # and the q row of each residual draw cross the link (the residual
-        # count of each timed seed is taken from an untimed device call).
-        n_cpu = h["num_draft"].long()
-        valid = (n_cpu >= 0) & (n_cpu <= K)
-        rows = torch.where(valid, n_cpu + 1, torch.ones_like(n_cpu))
-        esz = h["target_logits"].element_size()
-        h2d = int(rows.sum()) * V * esz
-        h2d += sum(t.numel() * t.element_size()
-                   for t in (h["draft_ids"], h["num_draft"], h["temperature"]))
-        if h["draft_probs"] is not None:
-            h2d += int(torch.where(valid, n_cpu, torch.zeros_like(n_cpu)).sum()) * 4
-            samp = (h["temperature"] > 0) & valid
-            n_res = 0
-            for i in range(e2e_steps):
-                _, nacc_i = binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids,
-                                                w.num_draft, w.temperature, 5000 + i)
-                n_res += int(((nacc_i.cpu().long() < n_cpu) & samp & (nacc_i.cpu() >= 0)).sum())
-            h2d += int(round(n_res / e2e_steps)) * V * 4
-        d2h = h_out.numel() * 4 + h_nacc.numel() * 4
-        e2e = {"value": world * pos / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+    # ---- every workload: per_config (rank 0 only)
+    per_config = None
+    if rank == 0 and not args.no_per_config:
+        per_config = {}
+        n_pc = max(3, min(args.steps, 30))
+        for cid in (1, 2, 3, 4, 5):
+            wc = w if (cid == args.config and not args.batch) else W.make_workload(cid, device=dev)
+            ent = measure_config(wc, dev, 0, n_pc, stream, flush, peak)
+            if not args.no_cpu:
+                for thr, key in ((1, "oracle_1t"), (0, "oracle_all_cores")):
+                    import oracle
+                    t_used = 1 if thr == 1 else oracle.omp_threads()
+                    rate, sample = oracle_rate(wc, thr, args.oracle_seconds)
+                    ent[key] = {"positions_per_s": round(rate, 1), "threads": t_used,
+                                "sample": sample}
+            per_config[f"config{cid}"] = ent
+            if cid == 5:
+                for (_, bb) in SWEEP:
+                    ws_ = wc.leading(bb)
+                    per_config[f"config5_B{bb}"] = measure_config(ws_, dev, 0, n_pc, stream,
+                                                                  flush, peak)
+                    del ws_
+            if wc is not w:
+                del wc
+            torch.cuda.empty_cache()
 
     cpu = None
+    parity_line = None
     if rank == 0 and not args.no_cpu:
         cpu = cpu_baseline(w, args.cpu_seconds)
+        parity_line = bench_parity(w, c)
 
     value = world * pos / (ms * 1e-3)
-    step_gbs = step_bytes / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
@@ -852,16 +944,97 @@ def main():
                              "device memory, written before each replay); ms_per_step_direct: "
                              "the same call launched directly"},
         "ms_per_step_direct": round(ms_direct, 5),
-        "hbm_gbs_step": round(step_gbs, 1), "hbm_frac_step": round(step_gbs / peak, 4),
-        "kernels_ms": {n: round(t, 5) for n, t in zip(names, kern_ms)},
-        "accept_rate": float(nacc_cpu.clamp(min=0).sum()) / max(1, pos),
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "ms_per_step_all_rows": round(ms_all_rows, 5),
+        "hbm_gbs_step": round(gate_gbs, 1), "hbm_frac_step": round(gate_gbs / peak, 4),
+        "hbm_step_bytes": int(by["algorithmic"]),
+        "literal_bytes": {"bytes": int(by["literal"]), "gbs": round(literal_gbs, 1),
+                          "frac": round(literal_gbs / peak, 4),
+                          "definition": "logits rows 0..n_b + draft probability rows "
+                                        "0..n_b-1, each read once"},
+        "bytes_read_per_step": int(by["read"]),
+        "kernels_ms": {n: round(t, 5) for n, t in zip(binding.KERNELS, kern_ms)},
+        "accept_rate": float(nacc_log.clamp(min=0).sum()) / max(1, pos * nacc_log.shape[0]),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "parity": parity_line,
+        "per_config": per_config,
         "gpu_launches": binding.N_KERNELS * args.steps, "clocks": clocks,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def bench_parity(w, c):
+    """Outputs of one GPU call against the oracle on the same inputs and seed:
+    requests whose outputs are identical (near-tie classification is the
+    parity tests' job)."""
+    import oracle
+    from speculative_decoding_verification_51_gb300 import workloads as W
+    seed = 4242
+    c.direct(seed)
+    torch.cuda.synchronize()
+    inputs = W.to_numpy(w)
+    inputs["seed"] = seed
+    ref = oracle.spec_verify(**inputs)
+    ids, nacc = c.out_ids.cpu().numpy(), c.out_nacc.cpu().numpy()
+    same = (ids == ref["out_ids"]).all(1) & (nacc == ref["out_num_accepted"])
+    return {"seed": seed, "requests": int(w.B), "identical": int(same.sum()),
+            "differing": int((~same).sum())}
+
+
+def e2e_host(w, dev, stream, args, world, pos):
+    """The same metric through spec_verify_host: inputs in pinned host memory,
+    outputs copied back, all inside the timed region."""
+    from speculative_decoding_verification_51_gb300 import binding
+    B, K, V = w.B, w.K, w.V
+    h = {k: getattr(w, k).cpu().pin_memory() for k in
+         ("target_logits", "draft_probs", "draft_ids", "num_draft", "temperature")}
+    h_out = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    h_nacc = torch.empty((B,), dtype=torch.int32).pin_memory()
+    d_l = torch.empty_like(w.target_logits)
+    d_p = torch.empty_like(w.draft_probs)
+    small = torch.empty(binding.host_small_bytes(B, K), dtype=torch.uint8, device=dev)
+    ws = binding.new_workspace(B, K, V, dev)
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def host_step(seed):
+        binding.spec_verify_host(h["target_logits"], h["draft_probs"], h["draft_ids"],
+                                 h["num_draft"], h["temperature"], seed, h_out, h_nacc, d_l,
+                                 d_p, small, ws)
+
+    for i in range(2):
+        host_step(4000 + i)
+    torch.cuda.synchronize()
+    a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a_ev.record(stream)
+    for i in range(e2e_steps):
+        host_step(5000 + i)
+    b_ev.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a_ev.elapsed_time(b_ev) / e2e_steps
+    # Pinned (mapped) host buffers take the rows-only path of
+    # spec_verify_host: the logits rows 0..n_b, q_j(x_j) of every draft, and
+    # the q row of each residual draw cross the link (the residual count of
+    # each timed seed is taken from an untimed device call).
+    n_cpu = h["num_draft"].long()
+    valid = (n_cpu >= 0) & (n_cpu <= K)
+    rows = torch.where(valid, n_cpu + 1, torch.ones_like(n_cpu))
+    esz = h["target_logits"].element_size()
+    h2d = int(rows.sum()) * V * esz
+    h2d += sum(t.numel() * t.element_size()
+               for t in (h["draft_ids"], h["num_draft"], h["temperature"]))
+    h2d += int(torch.where(valid, n_cpu, torch.zeros_like(n_cpu)).sum()) * 4
+    samp = (h["temperature"] > 0) & valid
+    n_res = 0
+    for i in range(e2e_steps):
+        _, nacc_i = binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids,
+                                        w.num_draft, w.temperature, 5000 + i)
+        n_res += int(((nacc_i.cpu().long() < n_cpu) & samp & (nacc_i.cpu() >= 0)).sum())
+    h2d += int(round(n_res / e2e_steps)) * V * 4
+    d2h = h_out.numel() * 4 + h_nacc.numel() * 4
+    return {"value": world * pos / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+            "path": "spec_verify_host (all-rows verifier over the copied rows)"}
 
 
 if __name__ == "__main__":

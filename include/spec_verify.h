@@ -42,6 +42,7 @@ extern "C" {
 
 /* Opaque CUDA stream (cudaStream_t); NULL is the legacy default stream. */
 typedef struct CUstream_st* spec_stream_t;
+typedef struct CUevent_st* spec_event_t;  /* a cudaEvent_t */
 
 typedef enum {
     SPEC_OK = 0,
@@ -106,6 +107,18 @@ size_t spec_verify_workspace_size(int B, int K, int V);
  *                    bytes, 256-byte aligned; the device status word lives in
  *                    it (spec_verify_status_ptr).
  *   stream           stream the kernels are enqueued on.
+ *
+ * Request b is verified the way the pages' loop runs ("RTP-LLM Speculative
+ * Engine", 拒绝采样算法: test draft j, break at the first rejection): rows
+ * 0..a_b are read, rows after the first rejection never are, and the rejected
+ * row is read a second time for the residual.  Every draft id j < n_b is
+ * range-checked first; a sampling row that is read and holds no finite logit
+ * makes the request bad (SPEC_BADBIT_EMPTY_ROW), a row that is never read is
+ * not checked (spec_verify_all_rows reads and checks rows 0..n_b).  When V
+ * exceeds 96 * 2048 tokens, or no CTA of the request-by-request kernel fits
+ * an SM, the call runs the all-rows verifier of spec_verify_all_rows instead.
+ * The call enqueues two kernels on `stream` (a one-CTA set-up kernel, then
+ * one persistent CTA per SM) and never synchronises.
  *
  * Sampling: p_j = softmax(l_j / T_b) is computed in float32 with float64
  * accumulation; accept x_j iff p_j(x_j) > 0 and (q_j(x_j) == 0 or
@@ -228,6 +241,35 @@ spec_status spec_verify_early_exit(const void* target_logits, spec_dtype logits_
                                    int32_t* dev_status, const uint64_t* seed_dev);
 
 /*
+ * spec_verify_all_rows -- the verification of spec_verify_ex, every row
+ * 0..num_draft[b] of every request read in one streaming pass.
+ *
+ * The pages' loop stops at the first rejection; this verifier reads the rows
+ * after it as well, so that the whole batch's row statistics come from one
+ * pass over the logits spread evenly over the GPU, then runs the acceptance
+ * tests, the residual masses and the draws as four more kernels.  Its outputs
+ * equal spec_verify's on the same inputs, except that every sampling row
+ * 0..num_draft[b] is checked for a finite logit (a row without one makes the
+ * request bad even if it lies after the first rejection), and dbg_rows hold
+ * {p_j(x_j), u_j, Z_j, accepted} for every draft row j < n_b of a sampling
+ * request.  Logit bytes read: sum_b (n_b + 1) V elem_size.
+ *   seed_dev  NULL (the seed is `seed`) or an 8-byte aligned device pointer
+ *             read in its place when the kernels run (for CUDA graph replay).
+ *   events    NULL, or six CUDA events recorded as in spec_verify_profiled.
+ * Other arguments, workspace (spec_verify_workspace_size), errors and the
+ * device status word as spec_verify_ex.
+ */
+spec_status spec_verify_all_rows(const void* target_logits, spec_dtype logits_dtype,
+                                 const float* draft_probs, const int32_t* draft_ids,
+                                 const int32_t* num_draft, const float* temperature,
+                                 uint64_t seed, int B, int K, int V, int32_t* out_ids,
+                                 int32_t* out_num_accepted, void* workspace,
+                                 size_t workspace_bytes, spec_stream_t stream,
+                                 uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                                 int32_t* dev_status, const uint64_t* seed_dev,
+                                 spec_event_t* events);
+
+/*
  * spec_lmhead_logits -- the target's logits from its last hidden states: the
  * vocabulary projection of the one target pass that scores the drafts
  * ("投机采样", 第二步: one forward of the target yields p_1 .. p_{gamma+1};
@@ -329,15 +371,17 @@ spec_status spec_verify_tree(const void* target_logits, spec_dtype logits_dtype,
 
 /*
  * spec_verify_profiled -- spec_verify with timing marks: the caller's CUDA
- * events events[0..5] (cudaEvent_t) are recorded on `stream` before each of
- * the five kernels of the call (plan; row statistics; acceptance tests;
- * residual masses; sampled tokens) and after the last, so that
- * events[i] -> events[i+1] brackets kernel i.
+ * events events[0..5] (cudaEvent_t) are recorded on `stream` around the
+ * kernels of the call, so that events[i] -> events[i+1] brackets kernel i.
+ * The request-by-request verifier runs two kernels: events[0] -> events[1]
+ * brackets the set-up kernel, events[1] -> events[2] the verifier, and
+ * events[2..5] are recorded together after it.  The all-rows verifier (see
+ * spec_verify_all_rows, which takes the same events) runs five: plan; row
+ * statistics; acceptance tests; residual masses; sampled tokens.
  * The marks separate the kernels, which otherwise overlap their launch with
  * the previous kernel's tail.  Returns SPEC_ERR_INVALID_ARG if any event is
  * NULL; otherwise as spec_verify.
  */
-typedef struct CUevent_st* spec_event_t;
 spec_status spec_verify_profiled(const void* target_logits, spec_dtype logits_dtype,
                                  const float* draft_probs, const int32_t* draft_ids,
                                  const int32_t* num_draft, const float* temperature,

@@ -22,8 +22,12 @@ BADBIT = {"num_draft": 1, "temperature": 2, "draft_id": 4, "empty_row": 8, "no_p
           "timeout": 32, "tree": 64}
 MODE_BAD, MODE_GREEDY, MODE_RESIDUAL, MODE_BONUS, MODE_FALLBACK, MODE_TYPICAL = -1, 0, 1, 2, 3, 4
 MAX_K = 31
-KERNELS = ("k_plan", "k_row_stats", "k_accept_all", "k_sample", "k_emit")  # launch order
+# kernels of one call, in launch order: spec_verify (request by request), and
+# the all-rows verifier (spec_verify_all_rows)
+KERNELS = ("k_prep", "k_verify")
+KERNELS_ALL_ROWS = ("k_plan", "k_row_stats", "k_accept_all", "k_sample", "k_emit")
 N_KERNELS = len(KERNELS)
+N_MARKS = 6  # events a profiled call records
 
 _LOCK = threading.Lock()
 _LIB = None
@@ -54,6 +58,8 @@ def _declare(lib):
                                          sz, vp, u32, vp, vp, vp]
     lib.spec_verify_early_exit.restype = i32
     lib.spec_verify_early_exit.argtypes = common + [u32, vp, vp, vp, vp]
+    lib.spec_verify_all_rows.restype = i32
+    lib.spec_verify_all_rows.argtypes = common + [u32, vp, vp, vp, vp, vp]
     lib.spec_verify_lmhead_workspace_size.restype = sz
     lib.spec_verify_lmhead_workspace_size.argtypes = [i32, i32, i32, i32]
     lib.spec_verify_lmhead.restype = i32
@@ -143,14 +149,18 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
                 out_num_accepted: torch.Tensor | None = None,
                 workspace: torch.Tensor | None = None, stream=None, request_offset: int = 0,
                 debug: bool = False, dev_status: torch.Tensor | None = None,
-                seed_dev: torch.Tensor | None = None, early_exit: bool = False):
+                seed_dev: torch.Tensor | None = None, early_exit: bool = False,
+                all_rows: bool = False):
     """Verify drafts on the GPU (see include/spec_verify.h for the semantics).
 
     seed_dev: a one-element int64 CUDA tensor; if given, the kernels read the
     seed from it when they run (spec_verify_dev_seed, for CUDA graph capture)
     and `seed` is ignored.
-    early_exit: read each request's rows only up to its first rejection, one
-    pass per draft position (spec_verify_early_exit); same outputs.
+    early_exit: the K + 1-pass form of reading each request's rows only up to
+    its first rejection (spec_verify_early_exit); same outputs.
+    all_rows: read and check every row 0..num_draft[b] in one streaming pass
+    (spec_verify_all_rows); same outputs except that an all -inf sampling row
+    after the first rejection makes the request bad.
     Returns (out_ids [B, K+1] int32, out_num_accepted [B] int32), plus
     (dbg_rows [B, K+1, 4], dbg_req [B, 4]) when debug=True.
     """
@@ -189,7 +199,14 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
         _check(seed_dev, "seed_dev", torch.int64, (1,), dev)
     with torch.cuda.device(dev):
         st = _stream(stream)
-        if early_exit:
+        if all_rows:
+            rc = lib().spec_verify_all_rows(
+                _p(target_logits), dt, _p(draft_probs), _p(draft_ids), _p(num_draft),
+                _p(temperature), ctypes.c_uint64(seed & (2**64 - 1)), B, K, V, _p(out_ids),
+                _p(out_num_accepted), _p(workspace), workspace.numel(), st,
+                ctypes.c_uint32(request_offset & 0xFFFFFFFF), _p(dbg_rows), _p(dbg_req),
+                _p(dev_status), _p(seed_dev), None)
+        elif early_exit:
             rc = lib().spec_verify_early_exit(
                 _p(target_logits), dt, _p(draft_probs), _p(draft_ids), _p(num_draft),
                 _p(temperature), ctypes.c_uint64(seed & (2**64 - 1)), B, K, V, _p(out_ids),
@@ -330,19 +347,26 @@ def spec_verify_tree(target_logits: torch.Tensor, draft_probs: torch.Tensor | No
 
 
 def spec_verify_profiled(target_logits, draft_probs, draft_ids, num_draft, temperature, seed,
-                         out_ids, out_num_accepted, workspace, events, stream=None) -> None:
-    """spec_verify with one torch.cuda.Event mark before each kernel and one after the last
-    (events must already have been recorded once, so that they exist)."""
+                         out_ids, out_num_accepted, workspace, events, stream=None,
+                         all_rows: bool = False) -> None:
+    """spec_verify (or, all_rows=True, spec_verify_all_rows) with N_MARKS
+    torch.cuda.Event marks around its kernels: events[i] -> events[i + 1]
+    brackets kernel i of KERNELS (KERNELS_ALL_ROWS).  The events must already
+    have been recorded once, so that they exist."""
     B, K1, V = target_logits.shape
     dt = SPEC_BF16 if target_logits.dtype == torch.bfloat16 else SPEC_F32
-    if len(events) != N_KERNELS + 1:
-        raise ValueError(f"need {N_KERNELS + 1} events")
+    if len(events) != N_MARKS:
+        raise ValueError(f"need {N_MARKS} events")
     handles = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     with torch.cuda.device(target_logits.device):
-        rc = lib().spec_verify_profiled(
-            _p(target_logits), dt, _p(draft_probs), _p(draft_ids), _p(num_draft),
-            _p(temperature), ctypes.c_uint64(seed & (2**64 - 1)), B, K1 - 1, V, _p(out_ids),
-            _p(out_num_accepted), _p(workspace), workspace.numel(), _stream(stream), handles)
+        args = (_p(target_logits), dt, _p(draft_probs), _p(draft_ids), _p(num_draft),
+                _p(temperature), ctypes.c_uint64(seed & (2**64 - 1)), B, K1 - 1, V, _p(out_ids),
+                _p(out_num_accepted), _p(workspace), workspace.numel(), _stream(stream))
+        if all_rows:
+            rc = lib().spec_verify_all_rows(*args, ctypes.c_uint32(0), None, None, None, None,
+                                            handles)
+        else:
+            rc = lib().spec_verify_profiled(*args, handles)
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify_profiled")
 

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
-SOURCES = ["plan.cu", "row_stats.cu", "sample.cu", "tree.cu", "lmhead.cu", "host_io.cu", "api.cu"]
+SOURCES = ["plan.cu", "row_stats.cu", "sample.cu", "verify.cu", "tree.cu", "lmhead.cu", "host_io.cu",
+           "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
 

@@ -51,7 +51,7 @@ __device__ __forceinline__ void merge_sum(float& m, float& z, float m2, float z2
         z = z2;
         z2 = tz;
     }
-    if (m2 != -INFINITY && z2 != 0.f) z = fmaf(z2, exp2f(rebase_arg(m2, m, kappa)), z);
+    if (m2 != -INFINITY && z2 != 0.f) z = fmaf(z2, rebase_factor(m2, m, kappa), z);
 }
 
 __device__ __forceinline__ void merge_argmax(float& m, int& a, float m2, int a2) {
@@ -87,7 +87,7 @@ __device__ __forceinline__ AccLoads accept_loads(const Params& P, int b, int n, 
 }
 
 // Step 1 for one row (whole warp; every lane gets the result): M = the row
-// max, Z = its normaliser against RN(M kappa), A = the lowest index of the
+// max, Z = its normaliser against offset_of(M, kappa), A = the lowest index of the
 // max (greedy rows).  With at most 128 chunks a lane's chunks stay in
 // registers: the max first (shuffles), then every chunk rebased onto it once
 // (one ex2 each) and summed (shuffles); longer rows merge pairwise.
@@ -133,7 +133,7 @@ __device__ __forceinline__ void merge_loaded(const Partial (&q)[MERGE_NPL], bool
 #pragma unroll
                 for (int i = 0; i < NPL; ++i)
                     if (q[i].m != -INFINITY && q[i].z != 0.0)
-                        lz = fmaf(float(q[i].z), ex2_approx(rebase_arg(q[i].m, M, kappa)), lz);
+                        lz = fmaf(float(q[i].z), rebase_factor(q[i].m, M, kappa), lz);
             }
             Z = warp_sum_f(lz);
         }

@@ -18,6 +18,8 @@ struct DeviceInfo {
     int stats_blocks_f32 = 0;
     int sample_blocks_bf16 = 0;  // resident k_sample CTAs per SM
     int sample_blocks_f32 = 0;
+    bool verify_bf16 = false;    // one k_verify CTA fits an SM
+    bool verify_f32 = false;
 };
 
 std::mutex g_mu;
@@ -70,6 +72,20 @@ spec_status device_info(DeviceInfo& out) {
                                                           SAMPLE_PAIRS * 64,
                                                           sample_smem(SPEC_F32)) != cudaSuccess)
             return SPEC_ERR_CUDA;
+        int vb = 0, vf = 0;
+        if (cudaFuncSetAttribute(k_verify_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(verify_smem(SPEC_BF16))) != cudaSuccess ||
+            cudaFuncSetAttribute(k_verify_f32, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(verify_smem(SPEC_F32))) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&vb, k_verify_bf16,
+                                                          verify_threads(SPEC_BF16),
+                                                          verify_smem(SPEC_BF16)) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&vf, k_verify_f32,
+                                                          verify_threads(SPEC_F32),
+                                                          verify_smem(SPEC_F32)) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+        d.verify_bf16 = vb >= 1;
+        d.verify_f32 = vf >= 1;
         d.stats_blocks_bf16 = d.stats_blocks_bf16 < 1 ? 1 : d.stats_blocks_bf16;
         d.stats_blocks_f32 = d.stats_blocks_f32 < 1 ? 1 : d.stats_blocks_f32;
         d.sample_blocks_bf16 = d.sample_blocks_bf16 < 1 ? 1 : d.sample_blocks_bf16;
@@ -91,9 +107,9 @@ constexpr bool kUsePdl = true;
 constexpr bool kUsePdl = false;
 #endif
 // Launches that use programmatic dependent launch whatever SV_PDL says (bit 0
-// k_row_stats, 1 k_accept_all, 2 k_sample, 3 k_emit).
+// k_row_stats, 1 k_accept_all, 2 k_sample, 3 k_emit, 4 k_verify).
 #ifndef SV_PDL_MASK
-#define SV_PDL_MASK 0
+#define SV_PDL_MASK 16
 #endif
 constexpr unsigned kPdlMask = SV_PDL_MASK;
 
@@ -134,7 +150,7 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
                            float threshold = 0.f, const int32_t* parents = nullptr,
                            int32_t* out_last = nullptr, const uint64_t* seed_dev = nullptr,
                            bool early_exit = false, const LmHeadIn* lm = nullptr,
-                           const float* host_probs = nullptr) {
+                           const float* host_probs = nullptr, bool all_rows = false) {
     const bool tree = parents != nullptr;
     if (!sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
     if (rule == RULE_TYPICAL && threshold != threshold) return SPEC_ERR_INVALID_ARG;
@@ -193,6 +209,27 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const bool bf16 = logits_dtype == SPEC_BF16;
+    // events (profiling only) are recorded before each kernel and after the last
+    auto mark = [&](int i) { return events ? cudaEventRecord(events[i], st) : cudaSuccess; };
+
+    // The request-by-request verifier (verify.cu): every lossless call whose
+    // rows fit its tile buffers, unless the caller asks for the all-rows pass.
+    const bool by_request = !all_rows && !tree && !early_exit && !lm && !host_probs &&
+                            rule == RULE_LOSSLESS && P.C <= VCMAX &&
+                            (bf16 ? dev.verify_bf16 : dev.verify_f32);
+    if (by_request) {
+        const long long gv = B < dev.sms ? B : dev.sms;
+        cudaError_t e = mark(0);
+        if (e == cudaSuccess) e = launch(k_prep, 1, 1024, 0, st, false, P);
+        if (e == cudaSuccess) e = mark(1);
+        if (e == cudaSuccess)
+            e = launch(bf16 ? k_verify_bf16 : k_verify_f32, unsigned(gv),
+                       unsigned(verify_threads(logits_dtype)), verify_smem(logits_dtype), st,
+                       true, P, 16u);
+        for (int i = 2; i <= 5 && e == cudaSuccess; ++i) e = mark(i);
+        return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    }
+
     const long long max_tiles = (long long)B * P.K1 * P.C;
     long long g1 = (long long)dev.sms * (bf16 ? dev.stats_blocks_bf16 : dev.stats_blocks_f32);
     const long long need1 = (max_tiles + STATS_WARPS - 1) / STATS_WARPS;
@@ -203,8 +240,6 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
     // k_emit: a warp per slot of the residual and of the bonus queue
     const unsigned g4 = unsigned((2LL * B + EMIT_WARPS - 1) / EMIT_WARPS);
 
-    // events (profiling only) are recorded before each kernel and after the last
-    auto mark = [&](int i) { return events ? cudaEventRecord(events[i], st) : cudaSuccess; };
     cudaError_t e = mark(0);
     if (e == cudaSuccess) e = launch(k_plan, 1, PLAN_THREADS, 0, st, false, P);
     if (e == cudaSuccess) e = mark(1);
@@ -333,6 +368,26 @@ spec_status spec_verify_early_exit(const void* target_logits, spec_dtype logits_
                        temperature, seed, B, K, V, out_ids, out_num_accepted, workspace,
                        workspace_bytes, stream, request_offset, dbg_rows, dbg_req, dev_status,
                        nullptr, RULE_LOSSLESS, 0.f, nullptr, nullptr, seed_dev, true);
+}
+
+spec_status spec_verify_all_rows(const void* target_logits, spec_dtype logits_dtype,
+                                 const float* draft_probs, const int32_t* draft_ids,
+                                 const int32_t* num_draft, const float* temperature,
+                                 uint64_t seed, int B, int K, int V, int32_t* out_ids,
+                                 int32_t* out_num_accepted, void* workspace,
+                                 size_t workspace_bytes, spec_stream_t stream,
+                                 uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                                 int32_t* dev_status, const uint64_t* seed_dev,
+                                 spec_event_t* events) {
+    if (reinterpret_cast<uintptr_t>(seed_dev) & 7) return SPEC_ERR_INVALID_ARG;
+    if (events)
+        for (int i = 0; i < 6; ++i)
+            if (!events[i]) return SPEC_ERR_INVALID_ARG;
+    return verify_impl(target_logits, logits_dtype, draft_probs, draft_ids, num_draft,
+                       temperature, seed, B, K, V, out_ids, out_num_accepted, workspace,
+                       workspace_bytes, stream, request_offset, dbg_rows, dbg_req, dev_status,
+                       reinterpret_cast<cudaEvent_t*>(events), RULE_LOSSLESS, 0.f, nullptr,
+                       nullptr, seed_dev, false, nullptr, nullptr, true);
 }
 
 size_t spec_verify_lmhead_workspace_size(int B, int K, int V, int H) {

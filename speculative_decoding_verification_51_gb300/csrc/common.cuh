@@ -62,8 +62,9 @@ constexpr int PLAN_THREADS = 1024;
 
 // HDR_ROUND + r: rows of early-exit round r (r >= 1), listed at rowlist + r * B
 // HDR_CLAIM: tail segments claimed so far in the all-rows pass of k_row_stats
-enum { HDR_ROWS = 0, HDR_NRES = 1, HDR_NBONUS = 2, HDR_STATUS = 3, HDR_CLAIM = 4, HDR_ROUND = 8,
-       HDR_INTS = 64 };
+// HDR_VCLAIM: requests claimed so far by k_verify's CTAs
+enum { HDR_ROWS = 0, HDR_NRES = 1, HDR_NBONUS = 2, HDR_STATUS = 3, HDR_CLAIM = 4, HDR_VCLAIM = 5,
+       HDR_ROUND = 8, HDR_INTS = 64 };
 static_assert(HDR_ROUND + SPEC_MAX_K + 1 <= HDR_INTS, "round counters overflow the header");
 enum { MODE_BAD = -1, MODE_GREEDY = 0, MODE_RESIDUAL = 1, MODE_BONUS = 2, MODE_FALLBACK = 3,
        MODE_TYPICAL = 4 };
@@ -232,16 +233,20 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // Token weights are w(x) = 2^((l(x) - m) kappa) for a reference maximum m.
-// With the offset c = RN(m * kappa) the exponent is one FFMA, l * kappa - c
-// (the product is exact inside the FMA); every weight of that reference then
-// carries the common factor 2^(m kappa - c), which cancels in every
-// normalised quantity.  The factor stays within 2^(+-1/2) while |c| < 2^24
-// (the rounding error of c is at most half an ulp <= 1/2); for larger |c|
-// (very small T, or very large logits) it would overflow or vanish, so the
-// two-operation form (l - m) * kappa, with no factor, is used instead.  Both
-// forms give 2^0 at l == m (up to the factor) and 0 far below it.
+// With the integer offset c = rint(RN(m * kappa)) the exponent is one FFMA,
+// l * kappa - c (the product is exact inside the FMA); every weight of that
+// reference then carries the common factor 2^(m kappa - c), which cancels in
+// every normalised quantity.  The factor stays within 2^(+-1) while
+// |c| < 2^24 (RN(m kappa) is then within 1/2 of m kappa, and c within 1/2 of
+// that); for larger |c| (very small T, or very large logits) it would overflow
+// or vanish, so the two-operation form (l - m) * kappa, with no factor, is
+// used instead.  Both forms give about 2^0 at l == m and 0 far below it.
+// Because offsets are integers, moving a sum from one reference to another is
+// multiplying it by an exact power of two (rebase_factor).
 constexpr float OFFSET_LIMIT = 16777216.f;  // 2^24
-__device__ __forceinline__ float offset_of(float m, float kappa) { return __fmul_rn(m, kappa); }
+__device__ __forceinline__ float offset_of(float m, float kappa) {
+    return rintf(__fmul_rn(m, kappa));
+}
 __device__ __forceinline__ bool offset_ok(float c) { return fabsf(c) < OFFSET_LIMIT; }
 __device__ __forceinline__ float weight_arg(float l, float m, float c, float kappa) {
     return offset_ok(c) ? fmaf(l, kappa, -c) : __fmul_rn(__fsub_rn(l, m), kappa);
@@ -250,7 +255,7 @@ __device__ __forceinline__ float weight_arg(float l, float m, float c, float kap
 // each reference with or without its offset as offset_ok decides: the exact
 // (m_c - m) kappa, less the factor 2^(m_c kappa - c_c) the weights of m_c
 // carry, plus the factor 2^(m kappa - c_m) those of m carry (both exact by
-// FMA).  With both offsets this is c_c - c_m.
+// FMA).  With both offsets this is the integer c_c - c_m.
 __device__ __forceinline__ float rebase_arg(float m_c, float m, float kappa) {
     const float cc = offset_of(m_c, kappa), cm = offset_of(m, kappa);
     const bool okc = offset_ok(cc), okm = offset_ok(cm);
@@ -259,6 +264,14 @@ __device__ __forceinline__ float rebase_arg(float m_c, float m, float kappa) {
     if (okc) r = __fsub_rn(r, fmaf(m_c, kappa, -cc));
     if (okm) r = __fadd_rn(r, fmaf(m, kappa, -cm));
     return r;
+}
+// 2^rebase_arg(m_c, m, kappa): with both offsets an exact power of two
+// (integer exponent, scaled in integer arithmetic), otherwise exp2f of the
+// mixed exponent.
+__device__ __forceinline__ float rebase_factor(float m_c, float m, float kappa) {
+    const float cc = offset_of(m_c, kappa), cm = offset_of(m, kappa);
+    if (offset_ok(cc) && offset_ok(cm)) return scalbnf(1.f, int(cc) - int(cm));
+    return exp2f(rebase_arg(m_c, m, kappa));
 }
 
 // Packed bf16x2 maximum (NaN operands lose).
@@ -381,6 +394,14 @@ __global__ void k_tree_walk_bf16(Params P);
 #endif
 constexpr int TREE_THREADS = SV_TREE_THREADS;
 constexpr int TREE_MAX_NODES = 32;
+
+// verify.cu: the request-by-request verifier (one persistent CTA per SM)
+constexpr int VCMAX = 96;  // longest row it takes, in 2048-token tiles (V <= 196608)
+__global__ void k_prep(Params P);
+__global__ void k_verify_bf16(Params P);
+__global__ void k_verify_f32(Params P);
+size_t verify_smem(int dtype);
+int verify_threads(int dtype);
 
 __global__ void k_philox_fill(uint64_t seed, const uint32_t* ctrs, int64_t n, uint32_t* out);
 

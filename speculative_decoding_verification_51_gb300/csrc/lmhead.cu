@@ -20,7 +20,7 @@
 // each row's logits at its slot, and in the same epilogue takes the
 // statistics k_row_stats would take from those logits: per (row, 2048-token
 // chunk) the maximum and, for sampling rows, the sum of 2^(l*kappa - c)
-// against c = RN(chunk max * kappa) (kept online over the chunk's 32-column
+// against c = offset_of(chunk max, kappa) (kept online over the chunk's 32-column
 // pieces, rescaled when the maximum grows), or for greedy rows the lowest
 // index of the maximum; l(x_j) and q(x_j) for the draft token.  All of it
 // is computed from the bf16-rounded logits that are stored, so the later
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                     } else {
                         if (pm > m_run) {  // rebase the running sum onto the new offset
                             if (z_run != 0.f)
-                                z_run = __fmul_rn(z_run, ex2_approx(rebase_arg(m_run, pm, kappa)));
+                                z_run = __fmul_rn(z_run, rebase_factor(m_run, pm, kappa));
                             m_run = pm;
                             c_run = offset_of(pm, kappa);
                         }

@@ -17,11 +17,11 @@
 // STATS_STAGES ahead while the warp reduces the current tile out of shared
 // memory (16-byte loads, 64 tokens per lane):
 //   sampling rows: each lane takes its maximum by a packed bf16x2 max tree and
-//     sums 2^(l * kappa - c) against its own offset c = RN(max * kappa) (one
+//     sums 2^(l * kappa - c) against its own offset c = rint(max * kappa) (one
 //     FFMA and one ex2 per token, pairwise float32 sums); the chunk maximum is
-//     one redux.sync, each lane's sum is rebased onto it with one ex2, and the
+//     one redux.sync, each lane's sum is rebased onto it by an exact power of two, and the
 //     lanes are summed by shuffles.  The stored sum is relative to the chunk's
-//     offset RN(chunk max * kappa), as every consumer expects;
+//     offset rint(chunk max * kappa), as every consumer expects;
 //   greedy rows: chunk max (redux), then the lowest index attaining it.
 // While the tile holding the draft token x_j of a row is in shared memory its
 // logit is copied out, and q_j(x_j) is fetched, for the acceptance test.
@@ -40,59 +40,11 @@
 
 #include "accept.cuh"
 #include "common.cuh"
+#include "stats.cuh"
 
 namespace sv {
 
 namespace {
-
-template <int DT>
-struct Tile {
-    static constexpr int ESZ = DT == SPEC_BF16 ? 2 : 4;   // bytes per logit
-    static constexpr int EPV = 16 / ESZ;                  // logits per 16-byte vector
-    static constexpr int BYTES = TILE * ESZ;              // one stage
-    static constexpr int VPL = TILE / EPV / 32;           // vectors per lane
-    static constexpr uint32_t NEG_INF_WORD = DT == SPEC_BF16 ? 0xFF80FF80u : 0xFF800000u;
-};
-
-template <int DT>
-__device__ __forceinline__ void unpack(const uint4& v, float (&f)[Tile<DT>::EPV]) {
-    if constexpr (DT == SPEC_BF16) {
-        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-        f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-        f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
-        f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-    } else {
-        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
-        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
-    }
-}
-
-// Maximum of a lane's VPL vectors (tree; packed bf16x2 for bf16).
-template <int DT>
-__device__ __forceinline__ float lane_max(const uint4 (&d)[Tile<DT>::VPL]) {
-    constexpr int VPL = Tile<DT>::VPL;
-    if constexpr (DT == SPEC_BF16) {
-        uint32_t w[VPL];
-#pragma unroll
-        for (int k = 0; k < VPL; ++k) w[k] = bmax2(bmax2(d[k].x, d[k].y), bmax2(d[k].z, d[k].w));
-#pragma unroll
-        for (int h = VPL / 2; h; h >>= 1)
-#pragma unroll
-            for (int k = 0; k < h; ++k) w[k] = bmax2(w[k], w[k + h]);
-        return fmaxf(bf16_lo(w[0]), bf16_hi(w[0]));
-    } else {
-        float w[VPL];
-#pragma unroll
-        for (int k = 0; k < VPL; ++k)
-            w[k] = fmaxf(fmaxf(__uint_as_float(d[k].x), __uint_as_float(d[k].y)),
-                         fmaxf(__uint_as_float(d[k].z), __uint_as_float(d[k].w)));
-#pragma unroll
-        for (int h = VPL / 2; h; h >>= 1)
-#pragma unroll
-            for (int k = 0; k < h; ++k) w[k] = fmaxf(w[k], w[k + h]);
-        return w[0];
-    }
-}
 
 // Per-row facts a warp needs while it streams the row's chunks.
 struct RowCtx {
@@ -129,84 +81,6 @@ __device__ __forceinline__ RowCtx row_ctx(const Params& P, const int* rowlist, l
 
 }  // namespace
 
-// The statistics of one staged tile (d: this lane's VPL vectors, nvec valid
-// vectors, tok0 the tile's first token): greedy rows the tile max and the
-// lowest index attaining it; sampling rows the tile max and the sum of
-// 2^(l kappa - c) against the tile max's offset c (see weight_arg).
-template <int DT>
-__device__ __forceinline__ Partial tile_partial(const uint4 (&d)[Tile<DT>::VPL], int nvec, int tok0,
-                                                const RowCtx& rc) {
-    constexpr int EPV = Tile<DT>::EPV, VPL = Tile<DT>::VPL;
-    const int lane = threadIdx.x & 31;
-    const float lmax = lane_max<DT>(d);
-    Partial out;
-    if (rc.greedy) {
-        // lowest index attaining the tile max: visiting tokens from high to
-        // low index leaves the lowest hit
-        const float m = redux_max_f32(lmax);
-        int bidx = INT_MAX;
-#pragma unroll
-        for (int k = VPL - 1; k >= 0; --k) {
-            if (k * 32 + lane < nvec) {
-                float f[EPV];
-                unpack<DT>(d[k], f);
-#pragma unroll
-                for (int e = EPV - 1; e >= 0; --e)
-                    if (f[e] == m) bidx = tok0 + (k * 32 + lane) * EPV + e;
-            }
-        }
-        out.m = m;
-        out.amax = redux_min_s32(bidx);
-        out.z = 0.0;
-    } else {
-        // each lane sums against its own maximum, so the ex2 loop does not
-        // wait for the warp-wide maximum; one rescale per lane follows
-        float zl = 0.f;
-        if (lmax != -INFINITY) {
-            const float cl = offset_of(lmax, rc.kappa);
-            float zs[VPL];
-            if (offset_ok(cl)) {  // one FFMA + ex2 per token
-#pragma unroll
-                for (int k = 0; k < VPL; ++k) {
-                    float f[EPV];
-                    unpack<DT>(d[k], f);
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) f[e] = ex2_approx(fmaf(f[e], rc.kappa, -cl));
-#pragma unroll
-                    for (int h = EPV / 2; h; h >>= 1)
-#pragma unroll
-                        for (int e = 0; e < h; ++e) f[e] = __fadd_rn(f[e], f[e + h]);
-                    zs[k] = f[0];
-                }
-            } else {  // offset too large (very small T): (l - max) * kappa
-#pragma unroll
-                for (int k = 0; k < VPL; ++k) {
-                    float f[EPV];
-                    unpack<DT>(d[k], f);
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e)
-                        f[e] = ex2_approx(__fmul_rn(__fsub_rn(f[e], lmax), rc.kappa));
-#pragma unroll
-                    for (int h = EPV / 2; h; h >>= 1)
-#pragma unroll
-                        for (int e = 0; e < h; ++e) f[e] = __fadd_rn(f[e], f[e + h]);
-                    zs[k] = f[0];
-                }
-            }
-#pragma unroll
-            for (int h = VPL / 2; h; h >>= 1)
-#pragma unroll
-                for (int k = 0; k < h; ++k) zs[k] = __fadd_rn(zs[k], zs[k + h]);
-            zl = zs[0];
-        }
-        const float m = redux_max_f32(lmax);
-        if (zl != 0.f) zl = __fmul_rn(zl, ex2_approx(rebase_arg(lmax, m, rc.kappa)));
-        out.m = m;
-        out.amax = -1;
-        out.z = double(warp_sum_f(zl));
-    }
-    return out;
-}
 
 
 // The all-rows pass (and a tree pass), balanced across SMs.  The streaming
@@ -359,7 +233,7 @@ __device__ __forceinline__ void stream_balanced(const Params& P, uint8_t* buf,
             fence_proxy_async_smem();
             issue(s);
         }
-        const Partial out = tile_partial<DT>(d, nvec, cc * TILE, rc);
+        const Partial out = tile_partial<DT>(d, nvec, cc * TILE, rc.greedy, rc.kappa);
         if (lane == 0) {
             P.part[(size_t)rc.slot * C + cc] = out;
             if (has_x) P.gath[rc.slot] = make_float2(lx, qx);
@@ -514,7 +388,7 @@ __device__ __forceinline__ void row_stats_body(const Params& P) {
             issue(s);
         }
 
-        const Partial out = tile_partial<DT>(d, nvec, cc * TILE, rc);
+        const Partial out = tile_partial<DT>(d, nvec, cc * TILE, rc.greedy, rc.kappa);
         if (lane == 0) {
             P.part[(size_t)rc.slot * P.C + cc] = out;
             if (has_x) P.gath[rc.slot] = make_float2(lx, qx);

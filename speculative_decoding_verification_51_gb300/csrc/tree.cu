@@ -138,11 +138,11 @@ __device__ __forceinline__ void tree_walk_body(const Params& P) {
             } else if (q.m != -INFINITY && q.z != 0.0) {
                 const float zc = float(q.z);
                 if (q.m > m) {
-                    if (m != -INFINITY && z != 0.f) z = __fmul_rn(z, exp2f(rebase_arg(m, q.m, kappa)));
+                    if (m != -INFINITY && z != 0.f) z = __fmul_rn(z, rebase_factor(m, q.m, kappa));
                     m = q.m;
                     z = __fadd_rn(z, zc);
                 } else {
-                    z = fmaf(zc, exp2f(rebase_arg(q.m, m, kappa)), z);
+                    z = fmaf(zc, rebase_factor(q.m, m, kappa), z);
                 }
             }
         }
@@ -158,11 +158,11 @@ __device__ __forceinline__ void tree_walk_body(const Params& P) {
                 }
             } else if (om != -INFINITY && oz != 0.f) {
                 if (om > m) {
-                    if (m != -INFINITY && z != 0.f) z = __fmul_rn(z, exp2f(rebase_arg(m, om, kappa)));
+                    if (m != -INFINITY && z != 0.f) z = __fmul_rn(z, rebase_factor(m, om, kappa));
                     m = om;
                     z = __fadd_rn(z, oz);
                 } else {
-                    z = fmaf(oz, exp2f(rebase_arg(om, m, kappa)), z);
+                    z = fmaf(oz, rebase_factor(om, m, kappa), z);
                 }
             }
         }

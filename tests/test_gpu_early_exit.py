@@ -1,11 +1,13 @@
-"""The early-exit verifier (spec_verify_early_exit, one pass per draft
-position, a request dropped at its first rejection) against the all-rows
-verifier and the float64 oracle (GPU).
+"""The verifiers that stop reading a request's rows at its first rejection
+(spec_verify, request by request in one persistent kernel, and
+spec_verify_early_exit, one pass per draft position) against the all-rows
+verifier (spec_verify_all_rows) and the float64 oracle (GPU).
 
-Both verifiers give every row they read the same arithmetic and the same
-Philox uniforms, so their outputs must be identical element by element, and
-so must the per-row diagnostics of every row the early-exit pass read (rows
-0..a_b); rows it never read report NaN with accept = -1.
+All three give every row they read the same arithmetic and the same Philox
+uniforms, so their outputs must be identical element by element, and so must
+the per-row diagnostics of every row both read (rows 0..a_b); rows the
+early-exit verifiers never read report NaN with accept = -1, and those two
+agree on every diagnostic.
 """
 import numpy as np
 import pytest
@@ -19,13 +21,18 @@ from speculative_decoding_verification_51_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _both(w, **kw):
-    par = run_gpu(w, **kw)
+def _all3(w, **kw):
+    """(all rows, K + 1 passes, request by request)"""
+    par = run_gpu(w, all_rows=True, **kw)
     ee = run_gpu(w, early_exit=True, **kw)
-    return par, ee
+    br = run_gpu(w, **kw)
+    return par, ee, br
 
 
-def _assert_same(w, par, ee):
+def _assert_same(w, par, ee, br=None):
+    if br is not None:  # the two early-exit verifiers agree on everything
+        for a, b in zip(ee, br):
+            assert np.array_equal(a, b, equal_nan=True)
     ids, nacc, rows, req = par
     ids2, nacc2, rows2, req2 = ee
     assert np.array_equal(nacc, nacc2)
@@ -45,8 +52,8 @@ def _assert_same(w, par, ee):
 @pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
 def test_early_exit_equals_all_rows(cid):
     w = W.make_workload(cid, device="cuda")
-    par, ee = _both(w)
-    _assert_same(w, par, ee)
+    par, ee, br = _all3(w)
+    _assert_same(w, par, ee, br)
     # the workload exercises early rejections, full acceptance and bonus rows
     nacc, n = par[1], w.num_draft.cpu().numpy()
     if cid >= 3:
@@ -68,15 +75,15 @@ def test_early_exit_more_seeds_and_offset():
     for s in (3, 4, 5):
         w = W.make_workload(4, device="cuda", gen_seed=100 + s)
         w.seed = 77 * s
-        par, ee = _both(w, request_offset=1000 * s)
-        _assert_same(w, par, ee)
+        par, ee, br = _all3(w, request_offset=1000 * s)
+        _assert_same(w, par, ee, br)
 
 
 def test_early_exit_k0_greedy_and_bad_requests():
     # K = 0: one pass, every request takes its bonus row
     w = W.make_workload(3, device="cuda", B=16, K=0, V=4096)
-    par, ee = _both(w)
-    _assert_same(w, par, ee)
+    par, ee, br = _all3(w)
+    _assert_same(w, par, ee, br)
     # all greedy, a bad draft id after the first rejection, a bad num_draft and
     # a bad temperature: flagged exactly as the all-rows pass flags them
     w = W.make_workload(5, device="cuda", B=32, V=8192)
@@ -90,11 +97,13 @@ def test_early_exit_k0_greedy_and_bad_requests():
     w.draft_ids, w.num_draft = ids, n
     st1 = torch.zeros(1, dtype=torch.int32, device="cuda")
     st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
-    par = run_gpu(w, dev_status=st1)
+    st3 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    par = run_gpu(w, all_rows=True, dev_status=st1)
     ee = run_gpu(w, early_exit=True, dev_status=st2)
-    _assert_same(w, par, ee)
+    br = run_gpu(w, dev_status=st3)
+    _assert_same(w, par, ee, br)
     assert par[1][3] == -1 and par[1][5] == -1 and par[1][6] == -1
-    assert int(st1.item()) == int(st2.item())
+    assert int(st1.item()) == int(st2.item()) == int(st3.item())
     s = int(st2.item())
     assert s & binding.BADBIT["draft_id"] and s & binding.BADBIT["num_draft"]
     assert s & binding.BADBIT["temperature"]
@@ -115,8 +124,11 @@ def test_early_exit_skips_rows_after_the_first_rejection():
     ref = run_gpu(w, early_exit=True)
     lg[2, 3, :] = float("-inf")          # request 2, row 3 (never read)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    par = run_gpu(w, dev_status=st)
+    par = run_gpu(w, dev_status=st, all_rows=True)
     ee = run_gpu(w, early_exit=True)
+    br = run_gpu(w)
+    for a, b in zip(ee, br):
+        assert np.array_equal(a, b, equal_nan=True)
     assert (ref[1] == 0).all()
     assert par[1][2] == -1 and int(st.item()) & binding.BADBIT["empty_row"]
     assert np.array_equal(ee[0], ref[0]) and np.array_equal(ee[1], ref[1])
@@ -171,8 +183,8 @@ def test_early_exit_31_drafts():
     n = np.where(np.arange(B) % 3 == 0, K, rng.integers(0, K + 1, B))
     T = np.where(np.arange(B) % 4 == 0, 0.0, 0.2)
     w = custom_workload(l, q, ids, n, T, bf16=True, seed=31)
-    par, ee = _both(w)
-    _assert_same(w, par, ee)
+    par, ee, br = _all3(w)
+    _assert_same(w, par, ee, br)
     assert par[1].max() >= 20  # some request got past pass 20
     rep = check_parity(w, "early_exit_K31", early_exit=True)
     assert not rep.failures, rep.failures[:5]
