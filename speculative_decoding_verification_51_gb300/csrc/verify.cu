@@ -104,6 +104,15 @@ struct VCtl {
 };
 
 __device__ __forceinline__ int vload(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+// A control word as lane 0 of the calling warp reads it, for every lane (all
+// 32 lanes call it): lanes that read a word another warp is changing each on
+// their own may see different values, and the warp's control flow splits.
+__device__ __forceinline__ int vload_w(const int* p) { return __shfl_sync(0xffffffffu, vload(p), 0); }
+// A bounded wait that started at t0 has run out, by lane 0's clock (all 32
+// lanes call it, so the warp leaves the wait as one).
+__device__ __forceinline__ bool waited_out(uint64_t t0) {
+    return __shfl_sync(0xffffffffu, int(globaltimer_ns() - t0 > VWAIT_NS), 0) != 0;
+}
 __device__ __forceinline__ void vstore(int* p, int v) { *reinterpret_cast<volatile int*>(p) = v; }
 
 __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
@@ -227,11 +236,11 @@ __device__ __forceinline__ float resid_tile_mass(const uint8_t* st, const uint8_
 
 // Bounded wait until pass p is published (false: abort or timeout).
 __device__ __forceinline__ bool wait_published(VCtl& S, int p, const Params& P) {
-    if (vload(&S.pub) > p) return true;
+    if (vload_w(&S.pub) > p) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (vload(&S.pub) <= p) {
-        if (vload(&S.abort)) return false;
-        if (globaltimer_ns() - t0 > VWAIT_NS) {
+    while (vload_w(&S.pub) <= p) {
+        if (vload_w(&S.abort)) return false;
+        if (waited_out(t0)) {
             vstore(&S.abort, 1);
             if ((threadIdx.x & 31) == 0) atomicOr(P.status, int(SPEC_BADBIT_TIMEOUT));
             return false;
@@ -265,7 +274,7 @@ __device__ __forceinline__ void v_stream(const Params& P, VCtl& S, Partial* bufs
 
     auto try_issue = [&]() {
         while (pend) {
-            if (ip >= vload(&S.pub)) break;
+            if (ip >= vload_w(&S.pub)) break;
             __threadfence_block();
             const VPass& d = S.desc[ip % VDRING];
             const int kind = d.kind;
@@ -413,13 +422,13 @@ __device__ __forceinline__ void v_prep(const Params& P, VCtl& S) {
     for (;;) {
         uint64_t t0 = globaltimer_ns();
         bool go = true;
-        while (vload(&S.want) <= given) {
-            if (vload(&S.abort)) {
-                go = false;
-                break;
-            }
-            if (globaltimer_ns() - t0 > VWAIT_NS) {
-                v_timeout(P, S);
+        for (;;) {  // lane 0 reads the shared flags: the warp takes one decision
+            int st = 0;  // 1 asked, 2 abort
+            if (lane == 0) st = vload(&S.want) > given ? 1 : vload(&S.abort) ? 2 : 0;
+            st = __shfl_sync(0xffffffffu, st, 0);
+            if (st == 1) break;
+            if (st == 2 || waited_out(t0)) {
+                if (st != 2) v_timeout(P, S);
                 go = false;
                 break;
             }
@@ -429,14 +438,18 @@ __device__ __forceinline__ void v_prep(const Params& P, VCtl& S) {
         int slot = -1;
         t0 = globaltimer_ns();
         while (slot < 0 && go) {  // the decider asks only while a record is free
-            for (int i = VREQ - 1; i >= 0; --i)
-                if (vload(&S.state[i]) == REQ_EMPTY) slot = i;
-            if (slot < 0) {
-                if (vload(&S.abort)) go = false;
-                else if (globaltimer_ns() - t0 > VWAIT_NS) {
-                    v_timeout(P, S);
-                    go = false;
-                }
+            int st = -1;
+            if (lane == 0) {
+                for (int i = VREQ - 1; i >= 0; --i)
+                    if (vload(&S.state[i]) == REQ_EMPTY) st = i;
+                if (st < 0 && vload(&S.abort)) st = -2;
+            }
+            st = __shfl_sync(0xffffffffu, st, 0);
+            if (st >= 0) slot = st;
+            else if (st == -2) go = false;
+            else if (waited_out(t0)) {
+                v_timeout(P, S);
+                go = false;
             }
         }
         if (!go) break;
@@ -572,11 +585,11 @@ __device__ __forceinline__ void v_decide(const Params& P, VCtl& S, const Partial
     // ask the prep warp for the next request, unless a claim is pending, a
     // request is already waiting, or every record is taken
     auto ask = [&]() {
-        if (vload(&S.given) != want || vload(&S.prep_done)) return;
+        if (vload_w(&S.given) != want || vload_w(&S.prep_done)) return;
         int taken = 0;
         bool ready = false;
         for (int i = 0; i < VREQ; ++i) {
-            const int st = vload(&S.state[i]);
+            const int st = vload_w(&S.state[i]);
             taken += st != REQ_EMPTY;
             ready |= st == REQ_READY;
         }
@@ -589,7 +602,7 @@ __device__ __forceinline__ void v_decide(const Params& P, VCtl& S, const Partial
     // has no drafts, and then the next request is asked for at once)
     auto activate = [&]() {
         for (int s = 0; s < VREQ; ++s) {
-            if (vload(&S.state[s]) != REQ_READY) continue;
+            if (vload_w(&S.state[s]) != REQ_READY) continue;
             __threadfence_block();
             if (lane == 0) vstore(&S.state[s], REQ_ACTIVE);
             __syncwarp();
@@ -768,7 +781,7 @@ __device__ __forceinline__ void v_decide(const Params& P, VCtl& S, const Partial
         } else {
             double total = 0.0;
             const int tok = draw_p(pp, b, n, M, kappa, R.u2[n], total);
-            if (vload(&S.abort)) return;
+            if (vload_w(&S.abort)) return;
             emit(s, n, tok, MODE_BONUS, total);
         }
         finish(s);
@@ -786,7 +799,7 @@ __device__ __forceinline__ void v_decide(const Params& P, VCtl& S, const Partial
         if (pk.chunk < 0) {  // a residual without mass: draw from p of row e instead
             double total = 0.0;
             const int tok = draw_p(bufs + S.debuf[s] * VCMAX, b, e, M, kappa, u2, total);
-            if (vload(&S.abort)) return;
+            if (vload_w(&S.abort)) return;
             emit(s, e, tok, MODE_FALLBACK, total);
             finish(s);
             return;
@@ -817,17 +830,17 @@ __device__ __forceinline__ void v_decide(const Params& P, VCtl& S, const Partial
         activate();
         if (fn == 0) {
             bool all_empty = true;
-            for (int i = 0; i < VREQ; ++i) all_empty &= vload(&S.state[i]) == REQ_EMPTY;
-            if (all_empty && vload(&S.prep_done)) {
+            for (int i = 0; i < VREQ; ++i) all_empty &= vload_w(&S.state[i]) == REQ_EMPTY;
+            if (all_empty && vload_w(&S.prep_done)) {
                 publish(PASS_END, 0, 0, 0, 0.f, 0.f);
                 break;
             }
             ask();
-            if (vload(&S.abort)) {
+            if (vload_w(&S.abort)) {
                 ok = false;
                 break;
             }
-            if (globaltimer_ns() - idle0 > VWAIT_NS) {
+            if (waited_out(idle0)) {
                 v_timeout(P, S);
                 ok = false;
                 break;
@@ -842,11 +855,11 @@ __device__ __forceinline__ void v_decide(const Params& P, VCtl& S, const Partial
         bool got = true;
         while (!__all_sync(0xffffffffu, mbar_try_wait(&S.done[buf], par))) {
             activate();
-            if (vload(&S.abort)) {
+            if (vload_w(&S.abort)) {
                 got = false;
                 break;
             }
-            if (globaltimer_ns() - t0 > VWAIT_NS) {
+            if (waited_out(t0)) {
                 v_timeout(P, S);
                 got = false;
                 break;
@@ -862,7 +875,7 @@ __device__ __forceinline__ void v_decide(const Params& P, VCtl& S, const Partial
         --fn;
         if (S.dkind[s] == PASS_ROW) on_row(s);
         else on_resid(s);
-        if (vload(&S.abort)) {
+        if (vload_w(&S.abort)) {
             ok = false;
             break;
         }

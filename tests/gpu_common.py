@@ -3,6 +3,7 @@ same seeded inputs."""
 from __future__ import annotations
 
 import json
+import math
 import os
 
 import numpy as np
@@ -48,6 +49,23 @@ def check_parity(w: W.Workload, tag: str, **kw) -> parity.Report:
                        "excused_cdf": rep.excused_cdf, "max_p_rel": rep.max_p_rel,
                        "failures": [str(x) for x in rep.failures[:20]]}, f, indent=1)
     return rep
+
+
+# Near-tie rate of the float32 inverse CDF.  Each of the V interval boundaries
+# of a draw sits within about 1e-8 of the row mass of its float64 place (the
+# pairwise float32 tile sums), and a uniform lands between the two with
+# probability equal to their gap, so a draw differs from the oracle's with
+# probability about 1e-8 V -- and then always inside the 1e-6 near-tie band.
+# Measured on the B=256, V=151936 workload over 50 calls: 11 in 9285 sampling
+# draws, 7.8e-9 V per draw.
+TIE_RATE_PER_TOKEN = 1e-8
+
+
+def assert_excused_within_rate(rep: parity.Report, V: int) -> None:
+    """The excused count of one call within the float32 near-tie rate: at most
+    lam + 4 sqrt(lam) + 1 for lam = TIE_RATE_PER_TOKEN * V * sampling draws."""
+    lam = TIE_RATE_PER_TOKEN * V * rep.sampling
+    assert rep.excused <= lam + 4.0 * math.sqrt(lam) + 1.0, (lam, rep.summary())
 
 
 def assert_excused_within_bound(rep: parity.Report) -> None:
