@@ -281,6 +281,48 @@ __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
     return r;
 }
 
+// Two float32 lanes in one 64-bit register for the packed sm_100-family
+// arithmetic (fma/add/mul/sub .rn.f32x2): each lane is rounded exactly as the
+// scalar instruction rounds it, so packed and scalar sums agree bit for bit
+// when they add in the same order.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// Sum of 8 floats in the order of the tree ((f0+f4)+(f2+f6)) + ((f1+f5)+(f3+f7)):
+// two packed adds, one packed add, one scalar add.
+__device__ __forceinline__ float sum8_tree(const float (&f)[8]) {
+    const uint64_t s = f2_add(f2_add(f2_pack(f[0], f[1]), f2_pack(f[4], f[5])),
+                              f2_add(f2_pack(f[2], f[3]), f2_pack(f[6], f[7])));
+    float a, b;
+    f2_unpack(s, a, b);
+    return __fadd_rn(a, b);
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

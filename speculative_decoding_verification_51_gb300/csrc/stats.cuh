@@ -100,18 +100,25 @@ __device__ __forceinline__ Partial tile_partial(const uint4 (&d)[Tile<DT>::VPL],
         if (lmax != -INFINITY) {
             const float cl = offset_of(lmax, kappa);
             float zs[VPL];
-            if (offset_ok(cl)) {  // one FFMA + ex2 per token
+            if (offset_ok(cl)) {  // one FFMA + ex2 per token, FFMAs and adds in pairs
+                const uint64_t kk = f2_pack(kappa, kappa), nc = f2_pack(-cl, -cl);
 #pragma unroll
                 for (int k = 0; k < VPL; ++k) {
                     float f[EPV];
                     unpack<DT>(d[k], f);
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e) f[e] = ex2_approx(fmaf(f[e], kappa, -cl));
-#pragma unroll
-                    for (int h = EPV / 2; h; h >>= 1)
-#pragma unroll
-                        for (int e = 0; e < h; ++e) f[e] = __fadd_rn(f[e], f[e + h]);
-                    zs[k] = f[0];
+                    for (int e = 0; e < EPV; e += 2) {
+                        f2_unpack(f2_fma(f2_pack(f[e], f[e + 1]), kk, nc), f[e], f[e + 1]);
+                        f[e] = ex2_approx(f[e]);
+                        f[e + 1] = ex2_approx(f[e + 1]);
+                    }
+                    if constexpr (EPV == 8) {
+                        zs[k] = sum8_tree(f);
+                    } else {
+                        float a, b;
+                        f2_unpack(f2_add(f2_pack(f[0], f[1]), f2_pack(f[2], f[3])), a, b);
+                        zs[k] = __fadd_rn(a, b);
+                    }
                 }
             } else {  // offset too large (very small T): (l - max) * kappa
 #pragma unroll
@@ -129,10 +136,12 @@ __device__ __forceinline__ Partial tile_partial(const uint4 (&d)[Tile<DT>::VPL],
                 }
             }
 #pragma unroll
-            for (int h = VPL / 2; h; h >>= 1)
+            for (int h = VPL / 2; h > 1; h >>= 1)  // the same tree, two sums per add
 #pragma unroll
-                for (int k = 0; k < h; ++k) zs[k] = __fadd_rn(zs[k], zs[k + h]);
-            zl = zs[0];
+                for (int k = 0; k < h; k += 2)
+                    f2_unpack(f2_add(f2_pack(zs[k], zs[k + 1]), f2_pack(zs[k + h], zs[k + h + 1])),
+                              zs[k], zs[k + 1]);
+            zl = __fadd_rn(zs[0], zs[1]);
         }
         const float m = redux_max_f32(lmax);
         if (zl != 0.f) zl = __fmul_rn(zl, rebase_factor(lmax, m, kappa));

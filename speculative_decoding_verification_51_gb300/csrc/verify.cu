@@ -124,7 +124,8 @@ __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
 // pass published, pass complete, request finished) with globaltimer stamps in
 // the workspace's tile-partial section, which this kernel does not otherwise
 // use: 256 records of 16 bytes per CTA (timing studies only; off by default).
-enum { TR_READY = 1, TR_PUB = 2, TR_DONE = 3, TR_FIN = 4, TR_PER_CTA = 256 };
+enum { TR_READY = 1, TR_PUB = 2, TR_DONE = 3, TR_FIN = 4, TR_SSTART = 5, TR_SLAND = 6,
+       TR_SARR = 7, TR_ENTRY = 11, TR_GO = 12, TR_PER_CTA = 256 };
 __device__ __forceinline__ void trace(const Params& P, int* count, int kind, int b, int row) {
 #ifdef SV_TRACE
     const int i = atomicAdd(count, 1);
@@ -329,11 +330,12 @@ __device__ __forceinline__ void v_stream(const Params& P, VCtl& S, Partial* bufs
         __threadfence_block();
         const VPass d = S.desc[p % VDRING];
         if (d.kind == PASS_END) break;
+        if (w == 0 && lane == 0) trace(P, &S.ntrace, TR_SSTART, d.b, d.kind * 100 + d.row);
         const bool rs = d.kind == PASS_RESID;
         const int ntiles = C > w ? (C - 1 - w) / NW + 1 : 0;
         Partial* out = bufs + d.buf * VCMAX;
         for (int t = 0; t < ntiles; ++t) {
-            try_issue();  // the tile is now in the FIFO (its pass is published)
+            if (fn == 0) try_issue();  // then the tile is in the FIFO (its pass is published)
             const uint32_t e = fifo & 1023u;
             fifo >>= 10;
             --fn;
@@ -345,18 +347,24 @@ __device__ __forceinline__ void v_stream(const Params& P, VCtl& S, Partial* bufs
             }
             phase ^= 1u << slot;
             busy &= ~(1u << slot);
+            if (t == 0 && w == 0 && lane == 0) trace(P, &S.ntrace, TR_SLAND, d.b, p);
             const int nel = min(TILE, V - c * TILE);
             const uint8_t* st = ring + slot * CF::SLOT;
             if (!rs) {
                 const int nvec = nel / EPV;
                 const uint4* v4 = reinterpret_cast<const uint4*>(st);
                 uint4 dv[VPL];
+                if (nvec == VPL * 32) {  // a full tile (every tile but a row's last)
 #pragma unroll
-                for (int k = 0; k < VPL; ++k) {
-                    const int v = k * 32 + lane;
-                    dv[k] = v < nvec ? v4[v]
-                                     : make_uint4(TL::NEG_INF_WORD, TL::NEG_INF_WORD,
-                                                  TL::NEG_INF_WORD, TL::NEG_INF_WORD);
+                    for (int k = 0; k < VPL; ++k) dv[k] = v4[k * 32 + lane];
+                } else {
+#pragma unroll
+                    for (int k = 0; k < VPL; ++k) {
+                        const int v = k * 32 + lane;
+                        dv[k] = v < nvec ? v4[v]
+                                         : make_uint4(TL::NEG_INF_WORD, TL::NEG_INF_WORD,
+                                                      TL::NEG_INF_WORD, TL::NEG_INF_WORD);
+                    }
                 }
                 const bool has_x = d.x >= 0 && d.x / TILE == c;
                 float lx = 0.f;
@@ -393,6 +401,7 @@ __device__ __forceinline__ void v_stream(const Params& P, VCtl& S, Partial* bufs
         try_issue();  // the producer leaves pass p before the pass can complete
         __syncwarp();
         if (lane == 0) mbar_arrive_cta(&S.done[d.buf]);
+        if (w == 0 && lane == 0) trace(P, &S.ntrace, TR_SARR, d.b, p);
     }
     if (!ok) {
         if (lane == 0) atomicOr(P.status, int(SPEC_BADBIT_TIMEOUT));
@@ -911,7 +920,9 @@ __device__ __forceinline__ void verify_body(const Params& P) {
         fence_mbarrier_init();
     }
     __syncthreads();
+    if (threadIdx.x == 0) trace(P, &S.ntrace, TR_ENTRY, 0, 0);
     griddep_wait();  // k_prep's claim order and cleared counter
+    if (threadIdx.x == 0) trace(P, &S.ntrace, TR_GO, 0, 0);
     if (warp < CF::NW)
         v_stream<DT>(P, S, bufs, smem + size_t(warp) * CF::RING, bars[warp], warp);
     else if (warp == CF::PREP)
