@@ -13,10 +13,12 @@ line (rank 0).
   e2e       same metric through spec_verify_host: from pinned host inputs
             only the rows the verifier reads are copied in, then verified,
             outputs copied back, all inside the timed region.
-  roofline  k_row_stats (the dominant kernel): algorithmic bytes per launch
-            (every valid logits row once + one 16-byte partial per
-            2048-token chunk) / its CUDA-event duration, against the measured
-            HBM copy bandwidth.
+  roofline  the dominant kernel of the verifier spec_verify runs for the
+            workload: k_verify when it verifies request by request (bytes:
+            rows 0..a_b of every request + the q row of each residual draw +
+            the small terms), k_row_stats when it runs the all-rows pass
+            (bytes: every valid logits row once); bytes per launch / its
+            CUDA-event duration, against the measured HBM copy bandwidth.
   cpu_baseline  the float64 oracle on the host cores, on a bounded sample.
 
 --impl reference times the oracle (the only reference this method has) on
@@ -674,7 +676,7 @@ class Caller:
     """One verification call on a workload, captured in a CUDA graph with the
     seed read from device memory (a step writes its seed, then replays)."""
 
-    def __init__(self, w, dev, offset, all_rows=False):
+    def __init__(self, w, dev, offset, all_rows=False, by_request=False):
         from speculative_decoding_verification_51_gb300 import binding
         self.w, self.dev, self.binding = w, dev, binding
         B, K, V = w.B, w.K, w.V
@@ -682,7 +684,7 @@ class Caller:
         self.out_ids = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
         self.out_nacc = torch.empty((B,), dtype=torch.int32, device=dev)
         self.seed_buf = torch.zeros(1, dtype=torch.int64, device=dev)
-        self.offset, self.all_rows = offset, all_rows
+        self.offset, self.all_rows, self.by_request = offset, all_rows, by_request
         cap = torch.cuda.Stream(dev)
         cap.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(cap):
@@ -699,14 +701,15 @@ class Caller:
                                  w.temperature, 0, out_ids=self.out_ids,
                                  out_num_accepted=self.out_nacc, workspace=self.ws,
                                  request_offset=self.offset, seed_dev=self.seed_buf, stream=st,
-                                 all_rows=self.all_rows)
+                                 all_rows=self.all_rows, by_request=self.by_request)
 
     def direct(self, seed):
         w = self.w
         self.binding.spec_verify(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
                                  w.temperature, seed, out_ids=self.out_ids,
                                  out_num_accepted=self.out_nacc, workspace=self.ws,
-                                 request_offset=self.offset, all_rows=self.all_rows)
+                                 request_offset=self.offset, all_rows=self.all_rows,
+                                 by_request=self.by_request)
 
 
 class L2Flush:
@@ -784,7 +787,9 @@ def measure_config(w, dev, offset, steps, stream, flush, peak):
     pos = W.positions(w.num_draft)
     valid = nacc_log >= 0
     acc = float((nacc_log.clamp(min=0)).sum()) / max(1, pos * nacc_log.shape[0])
+    path = c.binding.verify_path(w.B, w.K, w.V, w.target_logits.dtype, dev)
     out = {"B": w.B, "K": w.K, "V": w.V, "positions_per_call": pos,
+           "verifier": "request by request" if path else "all rows",
            "ms_per_call_cold_l2": round(ms_cold, 5), "ms_per_call_hot_l2": round(ms_hot, 5),
            "positions_per_s": round(pos / (ms_cold * 1e-3), 1),
            "accept_rate": round(acc, 4), "rows_all": by["rows_all"],
@@ -854,13 +859,17 @@ def run_chain(args, rank, world, local):
         devs[i][1].record(stream)
     torch.cuda.synchronize()
     ms_direct = statistics.mean(a.elapsed_time(b) for a, b in devs)
-    ca = Caller(w, dev, offset, all_rows=True)
-    for i in range(3):
-        flush(i)
-        ca.graph.replay()
-    torch.cuda.synchronize()
-    ms_all_rows = statistics.mean(time_replays(ca, n_aux, stream, flush)[0])
-    del ca
+    forced = {}
+    for name in ("all_rows", "by_request"):  # each verifier forced, at this workload
+        ca = Caller(w, dev, offset, **{name: True})
+        for i in range(3):
+            flush(i)
+            ca.graph.replay()
+        torch.cuda.synchronize()
+        forced[name] = statistics.mean(time_replays(ca, n_aux, stream, flush)[0])
+        del ca
+    path = binding.verify_path(B, K, V, w.target_logits.dtype, dev)
+    kernels = binding.KERNELS if path else binding.KERNELS_ALL_ROWS
 
     # ---- per-kernel durations (marks between the kernels of the call)
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(binding.N_MARKS)]
@@ -873,22 +882,29 @@ def run_chain(args, rank, world, local):
         flush(i + 3)
         binding.spec_verify_profiled(w.target_logits, w.draft_probs, w.draft_ids, w.num_draft,
                                      w.temperature, 3000 + i, c.out_ids, c.out_nacc, c.ws,
-                                     marks[i])
+                                     marks[i], by_request=bool(path), all_rows=not path)
     torch.cuda.synchronize()
     kern_ms = [statistics.mean(m[k].elapsed_time(m[k + 1]) for m in marks)
-               for k in range(binding.N_KERNELS)]
+               for k in range(len(kernels))]
 
-    # ---- bytes and the roofline of k_verify (the whole verification)
+    # ---- bytes and the roofline of the dominant kernel: k_verify (the whole
+    # verification) when the call runs request by request, else k_row_stats
     by = call_bytes(w, nacc_log)
     t_kern = kern_ms[1]
-    ach = by["read"] / (t_kern * 1e-3) / 1e9
     wname = workload_name(args.config, args.batch)
+    if path:
+        kb = by["read"]
+        kdef = ("rows 0..a_b of every request + the q row of each residual draw + gathers, "
+                "ids, counts and outputs")
+    else:
+        kb = by["rows_all"] * V * w.target_logits.element_size()
+        kdef = "every valid logits row 0..n_b once"
+    ach = kb / (t_kern * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(ach / peak, 4), "traffic": profiled_traffic(wname),
-                "kernel": "k_verify", "kernel_ms": round(t_kern, 5),
-                "algorithmic_bytes_per_launch": int(by["read"]),
-                "bytes_definition": "rows 0..a_b of every request + the q row of each "
-                                    "residual draw + gathers, ids, counts and outputs",
+                "frac": round(ach / peak, 4),
+                "traffic": profiled_traffic(wname) if path else None,
+                "kernel": kernels[1], "kernel_ms": round(t_kern, 5),
+                "algorithmic_bytes_per_launch": int(kb), "bytes_definition": kdef,
                 "peak_kind": peak_kind}
     gate_gbs = by["algorithmic"] / (ms * 1e-3) / 1e9
     literal_gbs = by["literal"] / (ms * 1e-3) / 1e9
@@ -942,9 +958,13 @@ def run_chain(args, rank, world, local):
                          "(L2 left full of clean unrelated lines)",
                    "launch": "one spec_verify call captured in a CUDA graph (seed read from "
                              "device memory, written before each replay); ms_per_step_direct: "
-                             "the same call launched directly"},
+                             "the same call launched directly",
+                   "verifier": ("request by request (k_prep + k_verify)" if path else
+                                "all rows (k_plan, k_row_stats, k_accept_all, k_sample, "
+                                "k_emit)")},
         "ms_per_step_direct": round(ms_direct, 5),
-        "ms_per_step_all_rows": round(ms_all_rows, 5),
+        "ms_per_step_all_rows": round(forced["all_rows"], 5),
+        "ms_per_step_by_request": round(forced["by_request"], 5),
         "hbm_gbs_step": round(gate_gbs, 1), "hbm_frac_step": round(gate_gbs / peak, 4),
         "hbm_step_bytes": int(by["algorithmic"]),
         "literal_bytes": {"bytes": int(by["literal"]), "gbs": round(literal_gbs, 1),
@@ -952,11 +972,11 @@ def run_chain(args, rank, world, local):
                           "definition": "logits rows 0..n_b + draft probability rows "
                                         "0..n_b-1, each read once"},
         "bytes_read_per_step": int(by["read"]),
-        "kernels_ms": {n: round(t, 5) for n, t in zip(binding.KERNELS, kern_ms)},
+        "kernels_ms": {n: round(t, 5) for n, t in zip(kernels, kern_ms)},
         "accept_rate": float(nacc_log.clamp(min=0).sum()) / max(1, pos * nacc_log.shape[0]),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "parity": parity_line,
         "per_config": per_config,
-        "gpu_launches": binding.N_KERNELS * args.steps, "clocks": clocks,
+        "gpu_launches": len(kernels) * args.steps, "clocks": clocks,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

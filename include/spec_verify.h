@@ -108,17 +108,24 @@ size_t spec_verify_workspace_size(int B, int K, int V);
  *                    it (spec_verify_status_ptr).
  *   stream           stream the kernels are enqueued on.
  *
- * Request b is verified the way the pages' loop runs ("RTP-LLM Speculative
- * Engine", 拒绝采样算法: test draft j, break at the first rejection): rows
- * 0..a_b are read, rows after the first rejection never are, and the rejected
- * row is read a second time for the residual.  Every draft id j < n_b is
- * range-checked first; a sampling row that is read and holds no finite logit
- * makes the request bad (SPEC_BADBIT_EMPTY_ROW), a row that is never read is
- * not checked (spec_verify_all_rows reads and checks rows 0..n_b).  When V
- * exceeds 96 * 2048 tokens, or no CTA of the request-by-request kernel fits
- * an SM, the call runs the all-rows verifier of spec_verify_all_rows instead.
- * The call enqueues two kernels on `stream` (a one-CTA set-up kernel, then
- * one persistent CTA per SM) and never synchronises.
+ * The call runs one of two verifiers with the same arithmetic and the same
+ * uniforms, whichever is faster for the batch (spec_verify_path tells which):
+ *   - request by request (spec_verify_by_request), once B is at least 1.6
+ *     times the device's SM count: request b is verified the way the pages'
+ *     loop runs ("RTP-LLM Speculative Engine", 拒绝采样算法: test draft j,
+ *     break at the first rejection), so rows 0..a_b are read, rows after the
+ *     first rejection never are, and the rejected row is read a second time
+ *     for the residual.  Two kernels: a one-CTA set-up kernel, then one
+ *     persistent CTA per SM.
+ *   - every row 0..n_b in one pass spread over the whole GPU
+ *     (spec_verify_all_rows), for smaller batches, and whenever V exceeds
+ *     96 * 2048 tokens or no CTA of the request-by-request kernel fits an SM.
+ *     Five kernels.
+ * Both give identical out_ids and out_num_accepted on valid inputs.  Every
+ * draft id j < n_b is range-checked first; a sampling row that the verifier
+ * reads and that holds no finite logit makes the request bad
+ * (SPEC_BADBIT_EMPTY_ROW): request by request checks rows 0..a_b, the
+ * all-rows pass rows 0..n_b.  The call never synchronises.
  *
  * Sampling: p_j = softmax(l_j / T_b) is computed in float32 with float64
  * accumulation; accept x_j iff p_j(x_j) > 0 and (q_j(x_j) == 0 or
@@ -268,6 +275,36 @@ spec_status spec_verify_all_rows(const void* target_logits, spec_dtype logits_dt
                                  uint32_t request_offset, float* dbg_rows, float* dbg_req,
                                  int32_t* dev_status, const uint64_t* seed_dev,
                                  spec_event_t* events);
+
+/*
+ * spec_verify_by_request -- the verification of spec_verify_ex request by
+ * request at any B ("RTP-LLM Speculative Engine", 拒绝采样算法: each request's
+ * drafts tested in order, stopping at the first rejection): one persistent
+ * CTA per SM claims whole requests, most drafts first, and reads a request's
+ * rows 0..a_b, then the rejected row again for the residual.  Logit bytes
+ * read: sum_b (a_b + 1) V elem_size, plus V * 4 for the q row of each
+ * residual draw.  dbg_rows hold NaN and accept = -1 for the rows after a_b,
+ * which are never read.  Falls back to the all-rows pass where its kernel
+ * does not apply (V > 96 * 2048, or no CTA fits an SM).  Arguments, events,
+ * workspace, errors and the device status word as spec_verify_all_rows.
+ */
+spec_status spec_verify_by_request(const void* target_logits, spec_dtype logits_dtype,
+                                   const float* draft_probs, const int32_t* draft_ids,
+                                   const int32_t* num_draft, const float* temperature,
+                                   uint64_t seed, int B, int K, int V, int32_t* out_ids,
+                                   int32_t* out_num_accepted, void* workspace,
+                                   size_t workspace_bytes, spec_stream_t stream,
+                                   uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                                   int32_t* dev_status, const uint64_t* seed_dev,
+                                   spec_event_t* events);
+
+/*
+ * spec_verify_path -- which verifier spec_verify (and spec_verify_ex,
+ * _profiled, _dev_seed, _noalloc) runs for these sizes on the current device:
+ * 1 request by request, 0 the all-rows pass, -1 invalid sizes or dtype, or a
+ * CUDA error while reading the device's properties.
+ */
+int spec_verify_path(int B, int K, int V, spec_dtype logits_dtype);
 
 /*
  * spec_lmhead_logits -- the target's logits from its last hidden states: the

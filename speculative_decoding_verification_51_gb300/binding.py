@@ -22,8 +22,9 @@ BADBIT = {"num_draft": 1, "temperature": 2, "draft_id": 4, "empty_row": 8, "no_p
           "timeout": 32, "tree": 64}
 MODE_BAD, MODE_GREEDY, MODE_RESIDUAL, MODE_BONUS, MODE_FALLBACK, MODE_TYPICAL = -1, 0, 1, 2, 3, 4
 MAX_K = 31
-# kernels of one call, in launch order: spec_verify (request by request), and
-# the all-rows verifier (spec_verify_all_rows)
+# kernels of one call, in launch order: the request-by-request verifier
+# (spec_verify_by_request, and spec_verify where verify_path() is 1), and the
+# all-rows verifier (spec_verify_all_rows, and spec_verify where it is 0)
 KERNELS = ("k_prep", "k_verify")
 KERNELS_ALL_ROWS = ("k_plan", "k_row_stats", "k_accept_all", "k_sample", "k_emit")
 N_KERNELS = len(KERNELS)
@@ -60,6 +61,10 @@ def _declare(lib):
     lib.spec_verify_early_exit.argtypes = common + [u32, vp, vp, vp, vp]
     lib.spec_verify_all_rows.restype = i32
     lib.spec_verify_all_rows.argtypes = common + [u32, vp, vp, vp, vp, vp]
+    lib.spec_verify_by_request.restype = i32
+    lib.spec_verify_by_request.argtypes = common + [u32, vp, vp, vp, vp, vp]
+    lib.spec_verify_path.restype = i32
+    lib.spec_verify_path.argtypes = [i32, i32, i32, i32]
     lib.spec_verify_lmhead_workspace_size.restype = sz
     lib.spec_verify_lmhead_workspace_size.argtypes = [i32, i32, i32, i32]
     lib.spec_verify_lmhead.restype = i32
@@ -150,7 +155,7 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
                 workspace: torch.Tensor | None = None, stream=None, request_offset: int = 0,
                 debug: bool = False, dev_status: torch.Tensor | None = None,
                 seed_dev: torch.Tensor | None = None, early_exit: bool = False,
-                all_rows: bool = False):
+                all_rows: bool = False, by_request: bool = False):
     """Verify drafts on the GPU (see include/spec_verify.h for the semantics).
 
     seed_dev: a one-element int64 CUDA tensor; if given, the kernels read the
@@ -161,6 +166,9 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
     all_rows: read and check every row 0..num_draft[b] in one streaming pass
     (spec_verify_all_rows); same outputs except that an all -inf sampling row
     after the first rejection makes the request bad.
+    by_request: the request-by-request verifier at any B
+    (spec_verify_by_request).  Without either flag the call runs the one
+    verify_path() names.
     Returns (out_ids [B, K+1] int32, out_num_accepted [B] int32), plus
     (dbg_rows [B, K+1, 4], dbg_req [B, 4]) when debug=True.
     """
@@ -199,8 +207,11 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
         _check(seed_dev, "seed_dev", torch.int64, (1,), dev)
     with torch.cuda.device(dev):
         st = _stream(stream)
-        if all_rows:
-            rc = lib().spec_verify_all_rows(
+        if all_rows or by_request:
+            if all_rows and by_request:
+                raise ValueError("all_rows and by_request exclude each other")
+            fn = lib().spec_verify_all_rows if all_rows else lib().spec_verify_by_request
+            rc = fn(
                 _p(target_logits), dt, _p(draft_probs), _p(draft_ids), _p(num_draft),
                 _p(temperature), ctypes.c_uint64(seed & (2**64 - 1)), B, K, V, _p(out_ids),
                 _p(out_num_accepted), _p(workspace), workspace.numel(), st,
@@ -348,10 +359,11 @@ def spec_verify_tree(target_logits: torch.Tensor, draft_probs: torch.Tensor | No
 
 def spec_verify_profiled(target_logits, draft_probs, draft_ids, num_draft, temperature, seed,
                          out_ids, out_num_accepted, workspace, events, stream=None,
-                         all_rows: bool = False) -> None:
-    """spec_verify (or, all_rows=True, spec_verify_all_rows) with N_MARKS
-    torch.cuda.Event marks around its kernels: events[i] -> events[i + 1]
-    brackets kernel i of KERNELS (KERNELS_ALL_ROWS).  The events must already
+                         all_rows: bool = False, by_request: bool = False) -> None:
+    """spec_verify (all_rows=True: spec_verify_all_rows; by_request=True:
+    spec_verify_by_request) with N_MARKS torch.cuda.Event marks around its
+    kernels: events[i] -> events[i + 1] brackets kernel i of KERNELS
+    (KERNELS_ALL_ROWS for the all-rows verifier).  The events must already
     have been recorded once, so that they exist."""
     B, K1, V = target_logits.shape
     dt = SPEC_BF16 if target_logits.dtype == torch.bfloat16 else SPEC_F32
@@ -362,13 +374,24 @@ def spec_verify_profiled(target_logits, draft_probs, draft_ids, num_draft, tempe
         args = (_p(target_logits), dt, _p(draft_probs), _p(draft_ids), _p(num_draft),
                 _p(temperature), ctypes.c_uint64(seed & (2**64 - 1)), B, K1 - 1, V, _p(out_ids),
                 _p(out_num_accepted), _p(workspace), workspace.numel(), _stream(stream))
-        if all_rows:
-            rc = lib().spec_verify_all_rows(*args, ctypes.c_uint32(0), None, None, None, None,
-                                            handles)
+        if all_rows or by_request:
+            fn = lib().spec_verify_all_rows if all_rows else lib().spec_verify_by_request
+            rc = fn(*args, ctypes.c_uint32(0), None, None, None, None, handles)
         else:
             rc = lib().spec_verify_profiled(*args, handles)
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify_profiled")
+
+
+def verify_path(B: int, K: int, V: int, dtype: torch.dtype, device=None) -> int:
+    """1 if spec_verify runs the request-by-request verifier for these sizes
+    on `device` (default: the current CUDA device), 0 if the all-rows pass."""
+    dt = SPEC_BF16 if dtype == torch.bfloat16 else SPEC_F32
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        r = lib().spec_verify_path(B, K, V, dt)
+    if r < 0:
+        raise SpecVerifyError(SPEC_ERR_INVALID_ARG, "spec_verify_path")
+    return r
 
 
 def status_word(workspace: torch.Tensor) -> torch.Tensor:

@@ -113,6 +113,19 @@ constexpr bool kUsePdl = false;
 #endif
 constexpr unsigned kPdlMask = SV_PDL_MASK;
 
+// Which verifier a lossless call runs: the caller's choice, or (PATH_AUTO)
+// the faster one for the batch.  The request-by-request kernel gives each
+// request one CTA, so it leaves SMs idle while B is small against the SM
+// count and each CTA's rows are read one after another; the all-rows pass
+// spreads every row over the whole GPU.  Measured on GB300 (152 SMs, V of
+// 129280 and 151936, bf16): request by request is faster from B of about
+// 1.6 x the SM count upward (B = 256: 0.079 vs 0.080 ms at K = 3, 0.113 vs
+// 0.112 ms at K = 8; B = 512, K = 8: 0.160 vs 0.184 ms), the all-rows pass
+// below it (B = 128: 0.068 vs 0.061 ms at K = 3; B = 8, K = 8: 0.081 vs
+// 0.043 ms).
+enum { PATH_AUTO = 0, PATH_ALL_ROWS = 1, PATH_BY_REQUEST = 2 };
+bool by_request_pays(long long B, int sms) { return 5 * B >= 8LL * sms; }
+
 cudaError_t launch(void (*kern)(Params), unsigned grid, unsigned block, size_t smem,
                    cudaStream_t st, bool pdl, const Params& P, unsigned pdl_bit = 0) {
     pdl = pdl && (kUsePdl || (kPdlMask & pdl_bit));
@@ -150,7 +163,7 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
                            float threshold = 0.f, const int32_t* parents = nullptr,
                            int32_t* out_last = nullptr, const uint64_t* seed_dev = nullptr,
                            bool early_exit = false, const LmHeadIn* lm = nullptr,
-                           const float* host_probs = nullptr, bool all_rows = false) {
+                           const float* host_probs = nullptr, int path = PATH_AUTO) {
     const bool tree = parents != nullptr;
     if (!sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
     if (rule == RULE_TYPICAL && threshold != threshold) return SPEC_ERR_INVALID_ARG;
@@ -214,9 +227,10 @@ static spec_status verify_impl(const void* target_logits, spec_dtype logits_dtyp
 
     // The request-by-request verifier (verify.cu): every lossless call whose
     // rows fit its tile buffers, unless the caller asks for the all-rows pass.
-    const bool by_request = !all_rows && !tree && !early_exit && !lm && !host_probs &&
-                            rule == RULE_LOSSLESS && P.C <= VCMAX &&
-                            (bf16 ? dev.verify_bf16 : dev.verify_f32);
+    const bool fits = !tree && !early_exit && !lm && !host_probs && rule == RULE_LOSSLESS &&
+                      P.C <= VCMAX && (bf16 ? dev.verify_bf16 : dev.verify_f32);
+    const bool by_request = fits && path != PATH_ALL_ROWS &&
+                            (path == PATH_BY_REQUEST || by_request_pays(B, dev.sms));
     if (by_request) {
         const long long gv = B < dev.sms ? B : dev.sms;
         cudaError_t e = mark(0);
@@ -387,7 +401,37 @@ spec_status spec_verify_all_rows(const void* target_logits, spec_dtype logits_dt
                        temperature, seed, B, K, V, out_ids, out_num_accepted, workspace,
                        workspace_bytes, stream, request_offset, dbg_rows, dbg_req, dev_status,
                        reinterpret_cast<cudaEvent_t*>(events), RULE_LOSSLESS, 0.f, nullptr,
-                       nullptr, seed_dev, false, nullptr, nullptr, true);
+                       nullptr, seed_dev, false, nullptr, nullptr, PATH_ALL_ROWS);
+}
+
+spec_status spec_verify_by_request(const void* target_logits, spec_dtype logits_dtype,
+                                   const float* draft_probs, const int32_t* draft_ids,
+                                   const int32_t* num_draft, const float* temperature,
+                                   uint64_t seed, int B, int K, int V, int32_t* out_ids,
+                                   int32_t* out_num_accepted, void* workspace,
+                                   size_t workspace_bytes, spec_stream_t stream,
+                                   uint32_t request_offset, float* dbg_rows, float* dbg_req,
+                                   int32_t* dev_status, const uint64_t* seed_dev,
+                                   spec_event_t* events) {
+    if (reinterpret_cast<uintptr_t>(seed_dev) & 7) return SPEC_ERR_INVALID_ARG;
+    if (events)
+        for (int i = 0; i < 6; ++i)
+            if (!events[i]) return SPEC_ERR_INVALID_ARG;
+    return verify_impl(target_logits, logits_dtype, draft_probs, draft_ids, num_draft,
+                       temperature, seed, B, K, V, out_ids, out_num_accepted, workspace,
+                       workspace_bytes, stream, request_offset, dbg_rows, dbg_req, dev_status,
+                       reinterpret_cast<cudaEvent_t*>(events), RULE_LOSSLESS, 0.f, nullptr,
+                       nullptr, seed_dev, false, nullptr, nullptr, PATH_BY_REQUEST);
+}
+
+int spec_verify_path(int B, int K, int V, spec_dtype logits_dtype) {
+    if (!sizes_ok(B, K, V) || V % 8 != 0) return -1;
+    if (logits_dtype != SPEC_F32 && logits_dtype != SPEC_BF16) return -1;
+    DeviceInfo dev;
+    if (device_info(dev) != SPEC_OK) return -1;
+    const bool fits = (V + TILE - 1) / TILE <= VCMAX &&
+                      (logits_dtype == SPEC_BF16 ? dev.verify_bf16 : dev.verify_f32);
+    return fits && by_request_pays(B, dev.sms) ? 1 : 0;
 }
 
 size_t spec_verify_lmhead_workspace_size(int B, int K, int V, int H) {

@@ -116,6 +116,36 @@ def test_early_exit_host_side_errors(lib):
     assert call(ws=0x80010) == bd.SPEC_ERR_WORKSPACE
 
 
+@pytest.mark.parametrize("entry", ["spec_verify_all_rows", "spec_verify_by_request"])
+def test_forced_path_host_side_errors(lib, entry):
+    """The two forced-path entry points check as spec_verify_ex does, plus
+    seed_dev alignment and a NULL entry among the events."""
+    from speculative_decoding_verification_51_gb300 import binding as bd
+    vp = ctypes.c_void_p
+    fn = getattr(lib, entry)
+
+    def call(B=2, K=3, V=64, seed_dev=None, ws=0x80000, events=None):
+        return fn(vp(0x10000), 1, vp(0x20000), vp(0x30000), vp(0x40000), vp(0x50000),
+                  ctypes.c_uint64(0), B, K, V, vp(0x60000), vp(0x70000), vp(ws), 1 << 30, vp(0),
+                  ctypes.c_uint32(0), None, None, None,
+                  None if seed_dev is None else vp(seed_dev), events)
+    assert call(K=32) == bd.SPEC_ERR_INVALID_ARG
+    assert call(V=1020) == bd.SPEC_ERR_UNSUPPORTED
+    assert call(B=0) == bd.SPEC_OK
+    assert call(seed_dev=0x90004) == bd.SPEC_ERR_INVALID_ARG
+    assert call(ws=0x80010) == bd.SPEC_ERR_WORKSPACE
+    ev = (ctypes.c_void_p * 6)(*([0x1000] * 5 + [0]))
+    assert call(events=ev) == bd.SPEC_ERR_INVALID_ARG
+
+
+def test_path_query_rejects_bad_sizes(lib):
+    """spec_verify_path answers -1 for sizes or dtypes no call accepts."""
+    assert lib.spec_verify_path(256, 32, 151936, 1) == -1   # K above the maximum
+    assert lib.spec_verify_path(256, 3, 1020, 1) == -1      # V not a multiple of 8
+    assert lib.spec_verify_path(256, 3, 151936, 7) == -1    # no such dtype
+    assert lib.spec_verify_path(-1, 3, 151936, 1) == -1
+
+
 def test_lmhead_host_side_errors(lib):
     """spec_lmhead_logits / spec_verify_lmhead reject bad sizes and pointers
     before any launch."""

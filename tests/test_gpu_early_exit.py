@@ -1,5 +1,5 @@
 """The verifiers that stop reading a request's rows at its first rejection
-(spec_verify, request by request in one persistent kernel, and
+(spec_verify_by_request, request by request in one persistent kernel, and
 spec_verify_early_exit, one pass per draft position) against the all-rows
 verifier (spec_verify_all_rows) and the float64 oracle (GPU).
 
@@ -25,7 +25,7 @@ def _all3(w, **kw):
     """(all rows, K + 1 passes, request by request)"""
     par = run_gpu(w, all_rows=True, **kw)
     ee = run_gpu(w, early_exit=True, **kw)
-    br = run_gpu(w, **kw)
+    br = run_gpu(w, by_request=True, **kw)
     return par, ee, br
 
 
@@ -100,7 +100,7 @@ def test_early_exit_k0_greedy_and_bad_requests():
     st3 = torch.zeros(1, dtype=torch.int32, device="cuda")
     par = run_gpu(w, all_rows=True, dev_status=st1)
     ee = run_gpu(w, early_exit=True, dev_status=st2)
-    br = run_gpu(w, dev_status=st3)
+    br = run_gpu(w, dev_status=st3, by_request=True)
     _assert_same(w, par, ee, br)
     assert par[1][3] == -1 and par[1][5] == -1 and par[1][6] == -1
     assert int(st1.item()) == int(st2.item()) == int(st3.item())
@@ -126,7 +126,7 @@ def test_early_exit_skips_rows_after_the_first_rejection():
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     par = run_gpu(w, dev_status=st, all_rows=True)
     ee = run_gpu(w, early_exit=True)
-    br = run_gpu(w)
+    br = run_gpu(w, by_request=True)
     for a, b in zip(ee, br):
         assert np.array_equal(a, b, equal_nan=True)
     assert (ref[1] == 0).all()

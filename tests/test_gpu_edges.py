@@ -90,8 +90,9 @@ def test_zero_target_probability_is_never_accepted():
     assert not np.any(out[:, 0] == 7)
 
 
-@pytest.mark.parametrize("all_rows", [False, True])
-def test_bad_inputs_flagged_and_isolated(all_rows):
+@pytest.mark.parametrize("path", ["auto", "all_rows", "by_request"])
+def test_bad_inputs_flagged_and_isolated(path):
+    kw = {} if path == "auto" else {path: True}
     rng = np.random.default_rng(2)
     B, K, V = 8, 2, 256
     l = rng.normal(0, 1, (B, K + 1, V))
@@ -103,7 +104,7 @@ def test_bad_inputs_flagged_and_isolated(all_rows):
     T = np.array([1.0, 1.0, 1.0, 1.0, np.nan, -0.5, 1.0, 0.0])
     w = custom_workload(l, q, ids, n, T, bf16=True, seed=1)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out, nacc, _, _ = run_gpu(w, dev_status=st, all_rows=all_rows)
+    out, nacc, _, _ = run_gpu(w, dev_status=st, **kw)
     bits = int(st.item())
     assert bits == (binding.BADBIT["num_draft"] | binding.BADBIT["temperature"] |
                     binding.BADBIT["draft_id"] | binding.BADBIT["empty_row"])
@@ -117,7 +118,7 @@ def test_bad_inputs_flagged_and_isolated(all_rows):
     w2 = custom_workload(l[[0, 7]], None, ids[[0, 7]], n[[0, 7]], T[[0, 7]], bf16=True)
     ensure_built()
     o2, n2 = binding.spec_verify(w2.target_logits, None, w2.draft_ids, w2.num_draft,
-                                 w2.temperature, 0, dev_status=st, all_rows=all_rows)
+                                 w2.temperature, 0, dev_status=st, **kw)
     assert int(st.item()) == binding.BADBIT["no_probs"]
     assert n2[0].item() == -1 and n2[1].item() == ref["out_num_accepted"][7]
 

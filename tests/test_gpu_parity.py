@@ -4,6 +4,7 @@ import pytest
 import torch
 
 from gpu_common import assert_excused_within_bound, assert_excused_within_rate, check_parity
+from speculative_decoding_verification_51_gb300 import binding
 from speculative_decoding_verification_51_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -35,3 +36,24 @@ def test_more_seeds(cid, seed):
     rep = check_parity(w, f"config{cid}_seed{seed}")
     assert not rep.failures, rep.failures[:5]
     assert_excused_within_rate(rep, w.V)
+
+
+@pytest.mark.parametrize("cid", [1, 2, 3])
+def test_workload_parity_by_request(cid):
+    """The smaller workloads, where spec_verify runs the all-rows pass, through
+    the request-by-request verifier."""
+    w = W.make_workload(cid, device="cuda")
+    rep = check_parity(w, f"config{cid}_by_request", by_request=True)
+    assert not rep.failures, rep.failures[:5]
+    assert rep.max_p_rel <= 1e-5
+    assert_excused_within_bound(rep)
+
+
+def test_path_follows_the_sm_count():
+    """spec_verify runs request by request from B = 1.6 x the SM count up."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    b0 = (8 * sms + 4) // 5  # the smallest B with 5 B >= 8 SMs
+    for B, want in ((b0 - 1, 0), (b0, 1), (512, 1), (64, 0), (1, 0)):
+        assert binding.verify_path(B, 3, 151936, torch.bfloat16) == want, (B, sms)
+    assert binding.verify_path(512, 3, 97 * 2048, torch.bfloat16) == 0  # rows too long
+    assert binding.verify_path(512, 3, 151936, torch.float32) == 1
