@@ -99,15 +99,17 @@ spec_status device_info(DeviceInfo& out) {
 // Programmatic dependent launch lets a kernel's launch and prologue overlap
 // its predecessor's tail; every kernel still executes griddepcontrol.wait
 // before it reads its predecessor's output, so either launch mode is correct.
-// Measured on GB300 with the four kernels of a call: plain stream order was
-// faster than programmatic dependent launch, so it is off unless -DSV_PDL.
-#ifdef SV_PDL
-constexpr bool kUsePdl = true;
-#else
+// Measured on GB300 for the all-rows pass (ms per call, plain order / PDL):
+// direct launches 0.0354 / 0.0285 (B=1), 0.0648 / 0.0563 (B=64, V=128256),
+// 0.0844 / 0.0740 (B=128, K=8); replays of a CUDA graph 0.0274 / 0.0287,
+// 0.0574 / 0.0561, 0.0746 / 0.0728.  On unless -DSV_NO_PDL.
+#ifdef SV_NO_PDL
 constexpr bool kUsePdl = false;
+#else
+constexpr bool kUsePdl = true;
 #endif
-// Launches that use programmatic dependent launch whatever SV_PDL says (bit 0
-// k_row_stats, 1 k_accept_all, 2 k_sample, 3 k_emit, 4 k_verify).
+// Launches that use programmatic dependent launch even under SV_NO_PDL (bit
+// 0 k_row_stats, 1 k_accept_all, 2 k_sample, 3 k_emit, 4 k_verify).
 #ifndef SV_PDL_MASK
 #define SV_PDL_MASK 16
 #endif
