@@ -97,24 +97,38 @@ def measured_peak():
         return PEAK_FALLBACK_GBS, "fallback", {}
 
 
-def verify_sha():
-    """Digest of the sources k_verify is compiled from."""
+# the sources each dominant kernel is compiled from, and the committed file
+# with its ncu DRAM bytes per launch
+KERNEL_SOURCES = {
+    "k_verify": (("verify.cu", "stats.cuh", "draw.cuh", "accept.cuh", "common.cuh"),
+                 "verify_traffic.json"),
+    "k_row_stats": (("row_stats.cu", "stats.cuh", "accept.cuh", "common.cuh"),
+                    "row_stats_traffic.json"),
+}
+
+
+def kernel_sha(kernel="k_verify"):
+    """Digest of the sources `kernel` is compiled from."""
     h = hashlib.sha256()
-    for f in ("verify.cu", "stats.cuh", "draw.cuh", "accept.cuh", "common.cuh"):
+    for f in KERNEL_SOURCES[kernel][0]:
         h.update(open(os.path.join(ROOT, "speculative_decoding_verification_51_gb300", "csrc", f),
                       "rb").read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload_name: str):
-    """ncu DRAM bytes per launch of k_verify for this workload, if the
+def verify_sha():
+    return kernel_sha("k_verify")
+
+
+def profiled_traffic(workload_name: str, kernel="k_verify"):
+    """ncu DRAM bytes per launch of `kernel` for this workload, if the
     committed summary was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "verify_traffic.json")
+    p = os.path.join(ROOT, "profiles", KERNEL_SOURCES[kernel][1])
     try:
         d = json.load(open(p))
     except Exception:
         return None
-    if d.get("source_sha") != verify_sha():
+    if d.get("source_sha") != kernel_sha(kernel):
         return None
     e = d.get("workloads", {}).get(workload_name)
     return None if e is None else float(e["dram_bytes_per_launch"])
@@ -902,7 +916,7 @@ def run_chain(args, rank, world, local):
     ach = kb / (t_kern * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4),
-                "traffic": profiled_traffic(wname) if path else None,
+                "traffic": profiled_traffic(wname, kernels[1]),
                 "kernel": kernels[1], "kernel_ms": round(t_kern, 5),
                 "algorithmic_bytes_per_launch": int(kb), "bytes_definition": kdef,
                 "peak_kind": peak_kind}

@@ -110,7 +110,7 @@ size_t spec_verify_workspace_size(int B, int K, int V);
  *
  * The call runs one of two verifiers with the same arithmetic and the same
  * uniforms, whichever is faster for the batch (spec_verify_path tells which):
- *   - request by request (spec_verify_by_request), once B is at least 1.6
+ *   - request by request (spec_verify_by_request), once B is at least 2.1
  *     times the device's SM count: request b is verified the way the pages'
  *     loop runs ("RTP-LLM Speculative Engine", 拒绝采样算法: test draft j,
  *     break at the first rejection), so rows 0..a_b are read, rows after the

@@ -119,14 +119,13 @@ constexpr unsigned kPdlMask = SV_PDL_MASK;
 // the faster one for the batch.  The request-by-request kernel gives each
 // request one CTA, so it leaves SMs idle while B is small against the SM
 // count and each CTA's rows are read one after another; the all-rows pass
-// spreads every row over the whole GPU.  Measured on GB300 (152 SMs, V of
-// 129280 and 151936, bf16): request by request is faster from B of about
-// 1.6 x the SM count upward (B = 256: 0.079 vs 0.080 ms at K = 3, 0.113 vs
-// 0.112 ms at K = 8; B = 512, K = 8: 0.160 vs 0.184 ms), the all-rows pass
-// below it (B = 128: 0.068 vs 0.061 ms at K = 3; B = 8, K = 8: 0.081 vs
-// 0.043 ms).
+// spreads every row over the whole GPU.  Measured on GB300 (152 SMs, bf16,
+// CUDA-graph replays, ms per call, by request / all rows): K = 8, V = 129280:
+// B = 256 0.1146 / 0.1099, B = 320 0.1290 / 0.1299, B = 384 0.1396 / 0.1527,
+// B = 512 0.1608 / 0.1961; K = 3, V = 151936, B = 256: 0.0791 / 0.0776.
+// Request by request from B of about 2.1 x the SM count.
 enum { PATH_AUTO = 0, PATH_ALL_ROWS = 1, PATH_BY_REQUEST = 2 };
-bool by_request_pays(long long B, int sms) { return 5 * B >= 8LL * sms; }
+bool by_request_pays(long long B, int sms) { return 10 * B >= 21LL * sms; }
 
 cudaError_t launch(void (*kern)(Params), unsigned grid, unsigned block, size_t smem,
                    cudaStream_t st, bool pdl, const Params& P, unsigned pdl_bit = 0) {
