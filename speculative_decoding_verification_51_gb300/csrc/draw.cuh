@@ -179,41 +179,72 @@ __device__ __forceinline__ Pick pick_chunk(int nc, float u, MassFn mass) {
     return pk;
 }
 
+// The reciprocal of d, an exact power of two of normal range, by its exponent
+// bits (the product by it then rounds as the quotient would); any other d is
+// divided as usual.
+__device__ __forceinline__ double pow2_recip(double d) {
+    const long long bits = __double_as_longlong(d);
+    const long long e = (bits >> 52) & 0x7FF;
+    if (e == 0 || e >= 2046 || (bits & 0xFFFFFFFFFFFFFLL) != 0) return 1.0 / d;
+    return __longlong_as_double((2046LL - e) << 52);
+}
+
+// Level-2 sums are fixed point: a weight w (0 <= w <= 4 by construction:
+// rebased token weights stay within 2^(+-1) of 1, residual weights are
+// probabilities) counts as the integer nearest w 2^48, so the running sums of
+// a chunk (2048 tokens, below 2^61) are exact integer additions: no float64
+// arithmetic, whose rate is low on this GPU, and each weight is off by at
+// most 2^-49.
+__device__ __forceinline__ long long fx48(float w) {
+    return w > 0.f ? __float2ll_rn(fminf(w, 4.f) * 0x1p48f) : 0LL;
+}
+// The level-2 target t in the same units: a running sum reaches t exactly
+// when the integer sum reaches ceil(t 2^48).  NaN never is reached.
+__device__ __forceinline__ long long fx48_target(double t) {
+    const double s = ceil(t * 0x1p48);
+    if (s != s || s >= 0x1p62) return 1LL << 62;
+    return s > 0.0 ? (long long)s : 0LL;
+}
+
 // Level 2 over a staged chunk of nel tokens starting at token c0: weight8(g, w)
 // gives the float32 weights of 8-token group g (same expression as level 1).
-// Groups are visited in token order g = 32 k + lane; the running sum is kept
-// in float64 (one warp per draw, so its cost is a few hundred additions);
-// returns the first token whose running sum reaches t, or the chunk's last
-// token of positive mass.
+// Groups are visited in token order g = 32 k + lane; the running sums are the
+// fixed-point sums above; returns the first token of positive weight whose
+// running sum reaches t, or the chunk's last token of positive weight.
 template <typename WeightFn>
 __device__ __forceinline__ int level2(int c0, int nel, double t, WeightFn weight8) {
     const int lane = threadIdx.x & 31;
     constexpr int G = TILE / 8 / 32;
+    const long long T = fx48_target(t);
     // block k by block k: the group sums of the block, their scan (carried
-    // from the blocks before), and a stop at the first block that reaches t
-    double carry = 0.0, before = 0.0;
-    int found = -1, last = -1;  // last: the last token of positive mass seen
+    // from the blocks before), and a stop at the first block that reaches T
+    long long carry = 0, before = 0;
+    int found = -1, last = -1;  // last: the last token of positive weight seen
 #pragma unroll 1
     for (int k = 0; k < G; ++k) {
         const int g = k * 32 + lane;
-        double gs = 0.0;
+        long long gs = 0;
+        bool pos = false;
         if (g * 8 < nel) {
             float w[8];
             weight8(g, w);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                gs += double(w[e]);
-                if (w[e] > 0.f) last = g * 8 + e;
+                gs += fx48(w[e]);
+                if (w[e] > 0.f) {
+                    last = g * 8 + e;
+                    pos = true;
+                }
             }
         }
-        double incl = gs;
+        long long incl = gs;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(0xffffffffu, incl, o);
+            const long long y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
         incl += carry;
-        const unsigned hit = __ballot_sync(0xffffffffu, incl >= t && gs > 0.0);
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= T && pos);
         if (hit) {
             const int l = __ffs(hit) - 1;
             found = k * 32 + l;
@@ -227,14 +258,14 @@ __device__ __forceinline__ int level2(int c0, int nel, double t, WeightFn weight
         if (lane == (found & 31)) {  // the owning lane walks its group
             float w[8];
             weight8(found, w);
-            double run = before;
+            long long run = before;
             int lastpos = -1;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                run += double(w[e]);
+                run += fx48(w[e]);
                 if (w[e] > 0.f) {
                     lastpos = found * 8 + e;
-                    if (x < 0 && run >= t) x = found * 8 + e;
+                    if (x < 0 && run >= T) x = found * 8 + e;
                 }
             }
             if (x < 0) x = lastpos;

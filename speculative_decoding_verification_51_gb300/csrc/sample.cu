@@ -101,7 +101,7 @@ __device__ __forceinline__ void emit_from_p(const Params& P, const ReqRec& rec, 
     }
     const Partial pc = part[pk.chunk];
     const double f_c = double(rebase_factor(pc.m, m, kappa));
-    const double t = (double(rec.u2) * pk.total - pk.before) / f_c;  // chunk-local mass
+    const double t = (double(rec.u2) * pk.total - pk.before) * pow2_recip(f_c);  // chunk-local
     const float cc = offset_of(pc.m, kappa);
     const int c0 = pk.chunk * TILE, nel = min(TILE, P.V - c0);
     const char* src = reinterpret_cast<const char*>(P.logits) +

@@ -699,7 +699,7 @@ __device__ __forceinline__ void v_decide(const Params& P, VCtl& S, const Partial
         if (pk.chunk < 0) return 0;  // no mass at all (not for a row with a finite logit)
         const Partial pc = part[pk.chunk];
         const double f_c = double(rebase_factor(pc.m, M, kappa));
-        const double t = (double(u2) * pk.total - pk.before) / f_c;
+        const double t = (double(u2) * pk.total - pk.before) * pow2_recip(f_c);
         const float cc = offset_of(pc.m, kappa);
         const int c0 = pk.chunk * TILE, nel = min(TILE, P.V - c0);
         const char* src = reinterpret_cast<const char*>(P.logits) +
