@@ -57,3 +57,17 @@ def test_path_follows_the_sm_count():
         assert binding.verify_path(B, 3, 151936, torch.bfloat16) == want, (B, sms)
     assert binding.verify_path(512, 3, 97 * 2048, torch.bfloat16) == 0  # rows too long
     assert binding.verify_path(512, 3, 151936, torch.float32) == 1
+
+
+def test_large_batch_by_request():
+    """Config 4's recipe at B = 1024: spec_verify verifies request by request,
+    each CTA claiming about seven requests in turn (the claim order, the two
+    request records and the pass ring reused many times)."""
+    w = W.make_workload(4, device="cuda", B=1024)
+    assert binding.verify_path(w.B, w.K, w.V, w.target_logits.dtype) == 1
+    rep = check_parity(w, "config4_B1024")
+    assert not rep.failures, rep.failures[:5]
+    assert rep.max_p_rel <= 1e-5
+    assert_excused_within_rate(rep, w.V)
+    del w
+    torch.cuda.empty_cache()
